@@ -1,0 +1,149 @@
+/*
+ * gbsort — device-wide sorting of fixed-length keys on NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of the CUDA library.  Every entry point takes plain pointers and
+ * sizes; device pointers are CUDA global-memory addresses on the current
+ * device, and `stream` is a cudaStream_t (CUstream) handle, NULL meaning the
+ * legacy default stream.  All work is enqueued on `stream`; no entry point
+ * synchronises the stream except gbs_get_status.
+ *
+ * Method (web pages, cited by title and section):
+ *  - LSD radix sort with 8-bit digits: per digit a histogram, an exclusive
+ *    prefix over the buckets and a STABLE scatter, lowest digit first
+ *    (kwkr.cn practice notes on bitonic sort vs LSD radix sort, §3.1-3.2;
+ *    "GPU基数排序：从CUB工程实现到性能调优", §3).
+ *  - Order-preserving key maps for signed integers and IEEE-754 floats
+ *    (kwkr.cn notes §3.3; "GPU基数排序", §5.2-5.3).
+ *  - Half-open bit ranges [begin_bit, end_bit), a size query with a NULL
+ *    work buffer, a reusable caller-owned work buffer, in-place calls
+ *    ("GPU基数排序", §2 and §6).
+ *  - Bitonic compare-exchange network, partner i^j, direction from the
+ *    segment bit (i & k), padding to a power of two with a maximal sentinel
+ *    ("并行排序：从归并网络到 GPU 双调排序", §3.3-3.5 and §4.2-4.3;
+ *    kwkr.cn notes §2.2-2.4 and §5.1).
+ *
+ * Ownership: the caller allocates and frees every buffer, including the work
+ * buffer `d_temp`.  The library allocates no memory on any sort call.
+ *
+ * Work-buffer protocol: call once with d_temp == NULL; *temp_bytes receives
+ * the size needed for these arguments and nothing is launched.  Then call
+ * with a device buffer of at least that many bytes (256-byte aligned) and
+ * *temp_bytes set to its size.  A buffer may be reused by later calls on the
+ * same stream; calls that share one buffer must not run concurrently.
+ *
+ * Errors: arguments are checked on the host before anything is launched and
+ * the call returns a status other than GBS_OK without touching memory.
+ * A CUDA launch failure returns GBS_ERR_CUDA.  Faults found on the device
+ * (a bounded wait that ran out) are recorded in the work buffer and
+ * reported by gbs_get_status.
+ */
+#ifndef GBSORT_H
+#define GBSORT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GBS_OK = 0,
+    GBS_ERR_INVALID_ARG = 1,    /* null pointer, bad bit range, bad key type, ... */
+    GBS_ERR_TEMP_TOO_SMALL = 2, /* *temp_bytes below the queried size */
+    GBS_ERR_UNSUPPORTED = 3,    /* size beyond the library's limits */
+    GBS_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
+    GBS_ERR_TIMEOUT = 5         /* a device-side bounded wait ran out */
+} gbs_status;
+
+typedef enum {
+    GBS_U32 = 0, /* uint32_t, sorted as unsigned */
+    GBS_I32 = 1, /* int32_t, two's complement; code = x ^ 0x80000000 */
+    GBS_F32 = 2, /* IEEE-754 binary32; code = b ^ (sign ? 0xFFFFFFFF : 0x80000000).
+                    -0.0 sorts before +0.0; -inf and +inf are the extremes;
+                    a NaN sorts by its bits (+NaN after +inf, -NaN before -inf). */
+    GBS_U64 = 3  /* uint64_t, sorted as unsigned */
+} gbs_key_type;
+
+/* Largest number of keys a radix sort call accepts: per-digit counts are
+ * kept in 29-bit fields of the tile status words. */
+#define GBS_MAX_RADIX_KEYS ((size_t)((1u << 29) - 1))
+/* Longest segment of gbs_segmented_sort (one CTA sorts one segment on chip). */
+#define GBS_MAX_SEGMENT_LEN ((size_t)16384)
+
+/*
+ * gbs_sort_keys — sort n keys by the bits [begin_bit, end_bit) of their code
+ * (the key itself for unsigned types, the order-preserving map above for i32
+ * and f32).  Equal codes keep their input order (stable; LSD radix sort:
+ * kwkr.cn notes §3.1, "GPU基数排序" §3).  Descending order (descending != 0)
+ * is the stable ascending order of the complemented code: keys
+ * non-increasing, equal keys in input order.  Output keys are the full
+ * original keys, bit for bit.
+ *   d_keys_in   device array of n keys (not modified unless equal to d_keys_out)
+ *   d_keys_out  device array of n keys; may equal d_keys_in (in place);
+ *               partial overlap is not allowed
+ *   n           number of keys, at most GBS_MAX_RADIX_KEYS
+ *   begin_bit, end_bit  0 <= begin_bit <= end_bit <= key width in bits;
+ *               begin_bit == end_bit copies the keys
+ * Small full-width calls (n <= GBS_MAX_SEGMENT_LEN, begin_bit == 0,
+ * end_bit == key width) run the one-CTA bitonic sorter; ties there are
+ * bit-identical keys, so the result equals the stable one.
+ */
+gbs_status gbs_sort_keys(void *d_temp, size_t *temp_bytes, gbs_key_type key_type,
+                         const void *d_keys_in, void *d_keys_out, size_t n,
+                         int begin_bit, int end_bit, int descending, void *stream);
+
+/*
+ * gbs_sort_pairs — like gbs_sort_keys, moving one uint32_t value with each
+ * key.  Stable: pairs with equal codes keep their input order.
+ *   d_vals_in / d_vals_out  device arrays of n uint32_t; may be equal
+ */
+gbs_status gbs_sort_pairs(void *d_temp, size_t *temp_bytes, gbs_key_type key_type,
+                          const void *d_keys_in, void *d_keys_out,
+                          const uint32_t *d_vals_in, uint32_t *d_vals_out, size_t n,
+                          int begin_bit, int end_bit, int descending, void *stream);
+
+/*
+ * gbs_segmented_sort — sort each of num_segments consecutive segments of
+ * segment_len keys independently, over the full key width, with the bitonic
+ * network ("并行排序" §3.3-3.5, §4.2-4.3).  A segment whose length is not a
+ * power of two is padded on chip with a sentinel that sorts after every key.
+ *   segment_len  1 .. GBS_MAX_SEGMENT_LEN (0 segments or length 0: no work)
+ *   d_keys_out may equal d_keys_in.
+ */
+gbs_status gbs_segmented_sort(void *d_temp, size_t *temp_bytes, gbs_key_type key_type,
+                              const void *d_keys_in, void *d_keys_out,
+                              size_t num_segments, size_t segment_len,
+                              int descending, void *stream);
+
+/*
+ * gbs_digit_histograms — the upfront digit histograms of a radix sort on
+ * their own: hist[p*256 + d] = number of keys whose digit p (bits
+ * [begin_bit + 8p, min(begin_bit + 8p + 8, end_bit)) of the code,
+ * complemented when descending) equals d (kwkr.cn notes §3.2, two-level
+ * counting).  d_hist receives ceil((end_bit - begin_bit) / 8) * 256 uint32_t.
+ * Same work-buffer protocol as gbs_sort_keys.
+ */
+gbs_status gbs_digit_histograms(void *d_temp, size_t *temp_bytes, gbs_key_type key_type,
+                                const void *d_keys, size_t n, int begin_bit, int end_bit,
+                                int descending, uint32_t *d_hist, void *stream);
+
+/*
+ * gbs_get_status — synchronises `stream`, then reports GBS_ERR_TIMEOUT if the
+ * last call that used this work buffer recorded a device-side timeout, else
+ * GBS_OK (GBS_ERR_CUDA if the stream reports an error).  temp_bytes is the
+ * size of d_temp.
+ */
+gbs_status gbs_get_status(const void *d_temp, size_t temp_bytes, void *stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *gbs_status_string(gbs_status status);
+
+/* Library version, e.g. "0.1.0" (static storage). */
+const char *gbs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBSORT_H */

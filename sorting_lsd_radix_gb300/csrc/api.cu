@@ -1,0 +1,275 @@
+// C ABI of the gbsort library: argument checks, work-buffer layout, dispatch
+// between the radix path and the bitonic tile sorter, status reporting.
+#include <cstring>
+
+#include "../../include/gbsort.h"
+#include "../../include/gbsort_debug.h"
+#include "launch.h"
+
+namespace {
+
+using gbs::Header;
+
+constexpr size_t ALIGN = 256;
+constexpr uint32_t DEFAULT_SPIN_LIMIT = 1u << 22;
+
+size_t round_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
+
+int key_bytes_of(gbs_key_type kt) {
+    switch (kt) {
+    case GBS_U32:
+    case GBS_I32:
+    case GBS_F32: return 4;
+    case GBS_U64: return 8;
+    default: return 0;
+    }
+}
+
+// test hooks (process-wide)
+int g_fault_pass = -1;
+uint32_t g_fault_tile = 0;
+uint32_t g_spin_limit = DEFAULT_SPIN_LIMIT;
+thread_local int t_launches = 0;
+thread_local void **t_events = nullptr;
+thread_local int t_event_count = 0;
+thread_local int t_event_next = 0;
+
+// Records events[0] before a call's first kernel (see gbs_debug_set_timing_events).
+void timing_start(cudaStream_t s) {
+    t_event_next = 0;
+    if (t_events && t_event_count > 0) cudaEventRecord(reinterpret_cast<cudaEvent_t>(t_events[t_event_next++]), s);
+}
+
+// Work-buffer layout of a radix call.
+struct Layout {
+    size_t hist, digit_base, status, keys_alt, vals_alt, total;
+    uint32_t num_tiles;
+};
+
+Layout radix_layout(int key_bytes, bool pairs, size_t n) {
+    Layout l;
+    const uint32_t tile = gbs::radix_tile_keys(key_bytes, pairs);
+    l.num_tiles = (uint32_t)((n + tile - 1) / tile);
+    size_t off = sizeof(Header);
+    l.hist = off;
+    off += round_up(sizeof(uint32_t) * gbs::MAX_PASSES * 256);
+    l.digit_base = off;
+    off += round_up(sizeof(uint32_t) * gbs::MAX_PASSES * 256);
+    l.status = off;
+    off += round_up(sizeof(uint32_t) * 256 * (size_t)l.num_tiles);
+    l.keys_alt = off;
+    off += round_up((size_t)key_bytes * n);
+    l.vals_alt = off;
+    if (pairs) off += round_up(sizeof(uint32_t) * n);
+    l.total = off;
+    return l;
+}
+
+gbs_status check_temp(void *d_temp, size_t *temp_bytes, size_t need, bool *query) {
+    *query = false;
+    if (temp_bytes == nullptr) return GBS_ERR_INVALID_ARG;
+    if (d_temp == nullptr) {
+        *temp_bytes = need;
+        *query = true;
+        return GBS_OK;
+    }
+    if ((reinterpret_cast<uintptr_t>(d_temp) % ALIGN) != 0) return GBS_ERR_INVALID_ARG;
+    if (*temp_bytes < need) return GBS_ERR_TEMP_TOO_SMALL;
+    return GBS_OK;
+}
+
+gbs_status from_cuda(cudaError_t e) { return e == cudaSuccess ? GBS_OK : GBS_ERR_CUDA; }
+
+cudaError_t copy_if_needed(const void *src, void *dst, size_t bytes, cudaStream_t s) {
+    if (src == dst || bytes == 0) return cudaSuccess;
+    return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s);
+}
+
+gbs_status radix_common(void *d_temp, size_t *temp_bytes, gbs_key_type kt, const void *keys_in, void *keys_out,
+                        const uint32_t *vals_in, uint32_t *vals_out, bool pairs, size_t n, int begin_bit,
+                        int end_bit, int descending, void *stream) {
+    t_launches = 0;
+    const int kb = key_bytes_of(kt);
+    if (kb == 0) return GBS_ERR_INVALID_ARG;
+    if (temp_bytes == nullptr) return GBS_ERR_INVALID_ARG;
+    if (begin_bit < 0 || end_bit < begin_bit || end_bit > 8 * kb) return GBS_ERR_INVALID_ARG;
+    if (n > GBS_MAX_RADIX_KEYS) return GBS_ERR_UNSUPPORTED;
+    const Layout lay = radix_layout(kb, pairs, n);
+    bool query = false;
+    gbs_status st = check_temp(d_temp, temp_bytes, lay.total, &query);
+    if (st != GBS_OK || query) return st;
+    if (n > 0 && (keys_in == nullptr || keys_out == nullptr)) return GBS_ERR_INVALID_ARG;
+    if (pairs && n > 0 && (vals_in == nullptr || vals_out == nullptr)) return GBS_ERR_INVALID_ARG;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned char *tb = reinterpret_cast<unsigned char *>(d_temp);
+    cudaError_t e = cudaMemsetAsync(tb, 0, lay.digit_base, s);  // header + histograms
+    if (e != cudaSuccess) return GBS_ERR_CUDA;
+
+    const int passes = (end_bit - begin_bit + 7) / 8;
+    if (n <= 1 || passes == 0) {
+        e = copy_if_needed(keys_in, keys_out, n * kb, s);
+        if (e == cudaSuccess && pairs) e = copy_if_needed(vals_in, vals_out, n * 4, s);
+        return from_cuda(e);
+    }
+    timing_start(s);
+    // small full-width key sorts: one CTA of the bitonic sorter
+    if (!pairs && n <= GBS_MAX_SEGMENT_LEN && begin_bit == 0 && end_bit == 8 * kb) {
+        e = gbs::launch_segmented_bitonic((int)kt, kb, keys_in, keys_out, 1, n, descending != 0, s, &t_launches);
+        return from_cuda(e);
+    }
+
+    gbs::RadixJob job;
+    job.kind = (int)kt;
+    job.key_bytes = kb;
+    job.pairs = pairs;
+    job.keys_in = keys_in;
+    job.keys_out = keys_out;
+    job.keys_alt = tb + lay.keys_alt;
+    job.vals_in = vals_in;
+    job.vals_out = vals_out;
+    job.vals_alt = pairs ? reinterpret_cast<uint32_t *>(tb + lay.vals_alt) : nullptr;
+    job.n = n;
+    job.begin_bit = begin_bit;
+    job.end_bit = end_bit;
+    job.num_passes = passes;
+    job.descending = descending != 0;
+    job.in_place = (keys_in == keys_out) || (pairs && vals_in == vals_out);
+    job.hdr = reinterpret_cast<Header *>(tb);
+    job.hist = reinterpret_cast<uint32_t *>(tb + lay.hist);
+    job.digit_base = reinterpret_cast<uint32_t *>(tb + lay.digit_base);
+    job.status = reinterpret_cast<uint32_t *>(tb + lay.status);
+    job.num_tiles = lay.num_tiles;
+    job.spin_limit = g_spin_limit;
+    job.fault_pass = g_fault_pass;
+    job.fault_tile = g_fault_tile;
+    return from_cuda(gbs::launch_radix_sort(job, s, &t_launches));
+}
+
+}  // namespace
+
+namespace gbs {
+void timing_mark(cudaStream_t s) {
+    if (t_events && t_event_next > 0 && t_event_next < t_event_count)
+        cudaEventRecord(reinterpret_cast<cudaEvent_t>(t_events[t_event_next++]), s);
+}
+}  // namespace gbs
+
+static_assert(GBS_MAX_RADIX_KEYS == gbs::STATUS_COUNT_MASK, "key limit must match the status count field");
+
+extern "C" {
+
+gbs_status gbs_sort_keys(void *d_temp, size_t *temp_bytes, gbs_key_type key_type, const void *d_keys_in,
+                         void *d_keys_out, size_t n, int begin_bit, int end_bit, int descending, void *stream) {
+    return radix_common(d_temp, temp_bytes, key_type, d_keys_in, d_keys_out, nullptr, nullptr, false, n, begin_bit,
+                        end_bit, descending, stream);
+}
+
+gbs_status gbs_sort_pairs(void *d_temp, size_t *temp_bytes, gbs_key_type key_type, const void *d_keys_in,
+                          void *d_keys_out, const uint32_t *d_vals_in, uint32_t *d_vals_out, size_t n,
+                          int begin_bit, int end_bit, int descending, void *stream) {
+    return radix_common(d_temp, temp_bytes, key_type, d_keys_in, d_keys_out, d_vals_in, d_vals_out, true, n,
+                        begin_bit, end_bit, descending, stream);
+}
+
+gbs_status gbs_segmented_sort(void *d_temp, size_t *temp_bytes, gbs_key_type key_type, const void *d_keys_in,
+                              void *d_keys_out, size_t num_segments, size_t segment_len, int descending,
+                              void *stream) {
+    t_launches = 0;
+    const int kb = key_bytes_of(key_type);
+    if (kb == 0 || temp_bytes == nullptr) return GBS_ERR_INVALID_ARG;
+    if (segment_len > GBS_MAX_SEGMENT_LEN) return GBS_ERR_UNSUPPORTED;
+    if (num_segments != 0 && segment_len != 0 && num_segments > (size_t)-1 / segment_len / 8)
+        return GBS_ERR_INVALID_ARG;
+    bool query = false;
+    gbs_status st = check_temp(d_temp, temp_bytes, sizeof(Header), &query);
+    if (st != GBS_OK || query) return st;
+    const size_t total = num_segments * segment_len;
+    if (total > 0 && (d_keys_in == nullptr || d_keys_out == nullptr)) return GBS_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(d_temp, 0, sizeof(Header), s);
+    if (e != cudaSuccess) return GBS_ERR_CUDA;
+    if (total == 0) return GBS_OK;
+    if (segment_len == 1) return from_cuda(copy_if_needed(d_keys_in, d_keys_out, total * kb, s));
+    timing_start(s);
+    return from_cuda(gbs::launch_segmented_bitonic((int)key_type, kb, d_keys_in, d_keys_out, num_segments,
+                                                   segment_len, descending != 0, s, &t_launches));
+}
+
+gbs_status gbs_digit_histograms(void *d_temp, size_t *temp_bytes, gbs_key_type key_type, const void *d_keys,
+                                size_t n, int begin_bit, int end_bit, int descending, uint32_t *d_hist,
+                                void *stream) {
+    t_launches = 0;
+    const int kb = key_bytes_of(key_type);
+    if (kb == 0 || temp_bytes == nullptr) return GBS_ERR_INVALID_ARG;
+    if (begin_bit < 0 || end_bit < begin_bit || end_bit > 8 * kb) return GBS_ERR_INVALID_ARG;
+    if (n > GBS_MAX_RADIX_KEYS) return GBS_ERR_UNSUPPORTED;
+    bool query = false;
+    gbs_status st = check_temp(d_temp, temp_bytes, sizeof(Header), &query);
+    if (st != GBS_OK || query) return st;
+    const int passes = (end_bit - begin_bit + 7) / 8;
+    if (passes == 0) return GBS_OK;
+    if (d_hist == nullptr || (n > 0 && d_keys == nullptr)) return GBS_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(d_temp, 0, sizeof(Header), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(d_hist, 0, sizeof(uint32_t) * 256 * passes, s);
+    if (e != cudaSuccess) return GBS_ERR_CUDA;
+    if (n == 0) return GBS_OK;
+    gbs::RadixJob job;
+    std::memset(&job, 0, sizeof(job));
+    job.kind = (int)key_type;
+    job.key_bytes = kb;
+    job.keys_in = d_keys;
+    job.n = n;
+    job.begin_bit = begin_bit;
+    job.end_bit = end_bit;
+    job.num_passes = passes;
+    job.descending = descending != 0;
+    job.hdr = reinterpret_cast<Header *>(d_temp);
+    job.hist = d_hist;
+    job.fault_pass = -1;
+    timing_start(s);
+    return from_cuda(gbs::launch_histograms(job, s, &t_launches));
+}
+
+gbs_status gbs_get_status(const void *d_temp, size_t temp_bytes, void *stream) {
+    if (d_temp == nullptr || temp_bytes < sizeof(Header)) return GBS_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return GBS_ERR_CUDA;
+    uint32_t err = 0;
+    if (cudaMemcpy(&err, d_temp, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess) return GBS_ERR_CUDA;
+    return err ? GBS_ERR_TIMEOUT : GBS_OK;
+}
+
+const char *gbs_status_string(gbs_status status) {
+    switch (status) {
+    case GBS_OK: return "GBS_OK";
+    case GBS_ERR_INVALID_ARG: return "GBS_ERR_INVALID_ARG";
+    case GBS_ERR_TEMP_TOO_SMALL: return "GBS_ERR_TEMP_TOO_SMALL";
+    case GBS_ERR_UNSUPPORTED: return "GBS_ERR_UNSUPPORTED";
+    case GBS_ERR_CUDA: return "GBS_ERR_CUDA";
+    case GBS_ERR_TIMEOUT: return "GBS_ERR_TIMEOUT";
+    default: return "GBS_ERR_UNKNOWN";
+    }
+}
+
+const char *gbs_version(void) { return "0.1.0"; }
+
+void gbs_debug_set_lookback_fault(int pass, uint32_t tile, uint32_t spin_limit) {
+    g_fault_pass = pass;
+    g_fault_tile = tile;
+    g_spin_limit = spin_limit ? spin_limit : DEFAULT_SPIN_LIMIT;
+}
+
+int gbs_debug_last_launch_count(void) { return t_launches; }
+
+void gbs_debug_set_timing_events(void **events, int count) {
+    t_events = events;
+    t_event_count = events ? count : 0;
+}
+
+size_t gbs_debug_radix_tile_keys(int key_bytes, int pairs) {
+    return gbs::radix_tile_keys(key_bytes, pairs != 0);
+}
+
+}  // extern "C"

@@ -1,0 +1,237 @@
+// Bitonic tile sorter: one CTA (or one warp, or one thread) sorts a segment of
+// up to 2^14 keys on chip.
+//
+// Network ("并行排序：从归并网络到 GPU 双调排序" §3.3-3.5, §4.2-4.3; kwkr.cn
+// notes on bitonic vs LSD radix sort §2.2-2.3): for merge size k = 2^m,
+// m = 1..log2(L), and stride j = k/2 .. 1, element i is compared with i ^ j;
+// the pair is put in ascending order when bit m of i is 0 (the segment bit,
+// taken from the index within the whole segment), descending otherwise.
+// Segments whose length is not a power of two are padded with the all-ones
+// code, which sorts after every key ("并行排序" §3.5; kwkr.cn notes §5.1).
+// Descending output sorts the complemented codes ascending.
+//
+// Mapping: each thread holds KP = 2^K_LOG keys in registers.  In the layout
+// with register-bit offset g0, register r of thread t holds the element whose
+// index bits [g0, g0 + K_LOG) are r and whose other bits are t's bits; every
+// stride 2^b with b in that range is then a compare-exchange between two
+// registers of one thread.  A stage walks its strides from the top bit down,
+// switching layout through shared memory (one store and one load per key)
+// whenever it crosses into the next group of K_LOG bits; the blocked layout
+// (g0 = 0) covers the K_LOG lowest bits.  Shared-memory rows are padded by one
+// element per 2^max(K_LOG, 4) so that both layouts are free of bank conflicts.
+#include <algorithm>
+
+#include "launch.h"
+
+namespace gbs {
+namespace {
+
+template <typename K, int L_LOG, int K_LOG> struct Shape {
+    static constexpr int L = 1 << L_LOG;
+    static constexpr int KP = 1 << K_LOG;
+    static constexpr int S = L / KP;               // threads per segment
+    static constexpr int T = S >= 128 ? S : 128;   // threads per CTA
+    static constexpr int SEGS = T / S;             // segments per CTA
+    static constexpr int PAD = K_LOG > 4 ? K_LOG : 4;  // one pad element per 2^PAD
+    static constexpr int LP = L + ((L >> PAD) > 0 ? (L >> PAD) : 1);  // padded row length (elements)
+    static constexpr bool WARP_LOCAL = S <= 32;
+    static constexpr size_t SMEM = (size_t)SEGS * LP * sizeof(K);
+};
+
+template <bool WARP_LOCAL> __device__ __forceinline__ void tile_sync() {
+    if (WARP_LOCAL)
+        __syncwarp();
+    else
+        __syncthreads();
+}
+
+// Index within the segment of register r of thread t in layout g0.
+template <int K_LOG> __device__ __forceinline__ int layout_index(int t, int r, int g0) {
+    return (t & ((1 << g0) - 1)) | (r << g0) | ((t >> g0) << (g0 + K_LOG));
+}
+
+template <int PAD> __device__ __forceinline__ int padded(int i) { return i + (i >> PAD); }
+
+template <typename K, int K_LOG, int PAD, bool WARP_LOCAL, int FROM, int TO>
+__device__ __forceinline__ void relayout(K (&x)[1 << K_LOG], K *row, int t) {
+    tile_sync<WARP_LOCAL>();
+#pragma unroll
+    for (int r = 0; r < (1 << K_LOG); ++r) row[padded<PAD>(layout_index<K_LOG>(t, r, FROM))] = x[r];
+    tile_sync<WARP_LOCAL>();
+#pragma unroll
+    for (int r = 0; r < (1 << K_LOG); ++r) x[r] = row[padded<PAD>(layout_index<K_LOG>(t, r, TO))];
+}
+
+// Compare-exchange across register bit RB in layout G0, for merge stage M.
+template <typename K, int K_LOG, int M, int G0, int RB>
+__device__ __forceinline__ void exchange_regbit(K (&x)[1 << K_LOG], int t) {
+#pragma unroll
+    for (int r = 0; r < (1 << K_LOG); ++r) {
+        if (r & (1 << RB)) continue;
+        const int r2 = r | (1 << RB);
+        bool desc;
+        if constexpr (M >= G0 && M < G0 + K_LOG)
+            desc = (r >> (M - G0)) & 1;      // segment bit is a register bit
+        else if constexpr (M < G0)
+            desc = (t >> M) & 1;             // ... a low thread bit
+        else
+            desc = (t >> (M - K_LOG)) & 1;   // ... a high thread bit
+        const K a = x[r], b = x[r2];
+        const K lo = a < b ? a : b;
+        const K hi = a < b ? b : a;
+        x[r] = desc ? hi : lo;
+        x[r2] = desc ? lo : hi;
+    }
+}
+
+template <typename K, int K_LOG, int M, int G0, int B>
+__device__ __forceinline__ void strides_down(K (&x)[1 << K_LOG], int t) {
+    exchange_regbit<K, K_LOG, M, G0, B - G0>(x, t);
+    if constexpr (B > G0) strides_down<K, K_LOG, M, G0, B - 1>(x, t);
+}
+
+// Register-bit offset of group q: q*K_LOG, kept inside the segment's index bits.
+template <int K_LOG, int L_LOG> __host__ __device__ constexpr int group_g0(int q) {
+    return q * K_LOG < L_LOG - K_LOG ? q * K_LOG : L_LOG - K_LOG;
+}
+
+// Stage M, register-bit group Q (top group QT first, down to group 0).  The
+// top group holds bit M-1; each lower group takes the bits below the one
+// above it.
+template <typename K, int K_LOG, int PAD, bool WARP_LOCAL, int L_LOG, int M, int Q, int QT>
+__device__ __forceinline__ void stage_groups(K (&x)[1 << K_LOG], K *row, int t) {
+    constexpr int G0 = group_g0<K_LOG, L_LOG>(Q);
+    constexpr int PREV = (Q == QT) ? 0 : group_g0<K_LOG, L_LOG>(Q + 1);
+    constexpr int HI = (Q == QT) ? M - 1 : PREV - 1;
+    static_assert(G0 >= 0 && G0 + K_LOG <= L_LOG && HI >= G0 && HI < G0 + K_LOG, "bad register-bit group");
+    if constexpr (G0 != PREV) relayout<K, K_LOG, PAD, WARP_LOCAL, PREV, G0>(x, row, t);
+    strides_down<K, K_LOG, M, G0, HI>(x, t);
+    if constexpr (Q > 0) stage_groups<K, K_LOG, PAD, WARP_LOCAL, L_LOG, M, Q - 1, QT>(x, row, t);
+}
+
+template <typename K, int K_LOG, int PAD, bool WARP_LOCAL, int L_LOG, int M>
+__device__ __forceinline__ void all_stages(K (&x)[1 << K_LOG], K *row, int t) {
+    if constexpr (M <= L_LOG) {
+        constexpr int QT = (M - 1) / K_LOG;
+        stage_groups<K, K_LOG, PAD, WARP_LOCAL, L_LOG, M, QT, QT>(x, row, t);
+        all_stages<K, K_LOG, PAD, WARP_LOCAL, L_LOG, M + 1>(x, row, t);
+    }
+}
+
+struct BitonicParams {
+    const void *keys_in;
+    void *keys_out;
+    size_t num_segments;
+    uint32_t seg_len;
+    int kind;
+    uint64_t flip;
+};
+
+template <typename K, int L_LOG, int K_LOG>
+__global__ void __launch_bounds__(Shape<K, L_LOG, K_LOG>::T) bitonic_tile_kernel(const BitonicParams prm) {
+    using Sh = Shape<K, L_LOG, K_LOG>;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    K *sm = reinterpret_cast<K *>(smem_raw);
+    const int tid = threadIdx.x;
+    const int t = tid % Sh::S;
+    K *row = sm + (tid / Sh::S) * Sh::LP;
+    const size_t seg0 = (size_t)blockIdx.x * Sh::SEGS;
+    const K *in = reinterpret_cast<const K *>(prm.keys_in);
+    K *out = reinterpret_cast<K *>(prm.keys_out);
+    const K flip = (K)prm.flip;
+    const uint32_t len = prm.seg_len;
+
+    // coalesced load of this CTA's segments, encoded, padded with all-ones
+    for (int e = tid; e < Sh::SEGS * Sh::L; e += Sh::T) {
+        const int s = e >> L_LOG, i = e & (Sh::L - 1);
+        const size_t seg = seg0 + s;
+        K v = KeyCodec<K>::ALL_ONES;
+        if (seg < prm.num_segments && (uint32_t)i < len) v = KeyCodec<K>::enc(in[seg * len + i], prm.kind, flip);
+        sm[s * Sh::LP + padded<Sh::PAD>(i)] = v;
+    }
+    __syncthreads();
+    K x[Sh::KP];
+#pragma unroll
+    for (int r = 0; r < Sh::KP; ++r) x[r] = row[padded<Sh::PAD>(layout_index<K_LOG>(t, r, 0))];
+
+    all_stages<K, K_LOG, Sh::PAD, Sh::WARP_LOCAL, L_LOG, 1>(x, row, t);
+
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < Sh::KP; ++r) row[padded<Sh::PAD>(layout_index<K_LOG>(t, r, 0))] = x[r];
+    __syncthreads();
+    for (int e = tid; e < Sh::SEGS * Sh::L; e += Sh::T) {
+        const int s = e >> L_LOG, i = e & (Sh::L - 1);
+        const size_t seg = seg0 + s;
+        if (seg < prm.num_segments && (uint32_t)i < len)
+            out[seg * len + i] = KeyCodec<K>::dec(sm[s * Sh::LP + padded<Sh::PAD>(i)], prm.kind, flip);
+    }
+}
+
+template <typename K, int L_LOG, int K_LOG>
+cudaError_t launch_shape(const BitonicParams &prm, cudaStream_t stream) {
+    using Sh = Shape<K, L_LOG, K_LOG>;
+    auto kern = bitonic_tile_kernel<K, L_LOG, K_LOG>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sh::SMEM);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const size_t grid = (prm.num_segments + Sh::SEGS - 1) / Sh::SEGS;
+    kern<<<(unsigned)grid, Sh::T, Sh::SMEM, stream>>>(prm);
+    return cudaGetLastError();
+}
+
+template <typename K, int L_LOG>
+cudaError_t launch_len(const BitonicParams &prm, cudaStream_t stream) {
+    // 32 keys per thread for 4-byte keys; 16 for 8-byte keys, except 32 at
+    // 2^14 keys, where 16 would need 1024 threads with at most 64 registers
+    constexpr int KMAX = (sizeof(K) == 8 && L_LOG < 14) ? 4 : 5;
+    constexpr int K_LOG = L_LOG < KMAX ? L_LOG : KMAX;
+    return launch_shape<K, L_LOG, K_LOG>(prm, stream);
+}
+
+template <typename K>
+cudaError_t launch_by_log(int l, const BitonicParams &prm, cudaStream_t stream) {
+    switch (l) {
+    case 1: return launch_len<K, 1>(prm, stream);
+    case 2: return launch_len<K, 2>(prm, stream);
+    case 3: return launch_len<K, 3>(prm, stream);
+    case 4: return launch_len<K, 4>(prm, stream);
+    case 5: return launch_len<K, 5>(prm, stream);
+    case 6: return launch_len<K, 6>(prm, stream);
+    case 7: return launch_len<K, 7>(prm, stream);
+    case 8: return launch_len<K, 8>(prm, stream);
+    case 9: return launch_len<K, 9>(prm, stream);
+    case 10: return launch_len<K, 10>(prm, stream);
+    case 11: return launch_len<K, 11>(prm, stream);
+    case 12: return launch_len<K, 12>(prm, stream);
+    case 13: return launch_len<K, 13>(prm, stream);
+    case 14: return launch_len<K, 14>(prm, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_segmented_bitonic(int kind, int key_bytes, const void *keys_in, void *keys_out,
+                                     size_t num_segments, size_t segment_len, bool descending,
+                                     cudaStream_t stream, int *launches) {
+    BitonicParams prm;
+    prm.keys_in = keys_in;
+    prm.keys_out = keys_out;
+    prm.num_segments = num_segments;
+    prm.seg_len = (uint32_t)segment_len;
+    prm.kind = kind;
+    prm.flip = descending ? ~0ull : 0ull;
+    int l = 0;
+    while ((size_t(1) << l) < segment_len) ++l;
+    ++*launches;
+    const cudaError_t e = key_bytes == 8 ? launch_by_log<uint64_t>(l, prm, stream)
+                                         : launch_by_log<uint32_t>(l, prm, stream);
+    timing_mark(stream);
+    return e;
+}
+
+}  // namespace gbs

@@ -1,0 +1,257 @@
+"""Python binding of the gbsort C ABI (include/gbsort.h).
+
+Argument marshalling only: every function forwards torch tensors' device
+pointers, sizes and the current CUDA stream to the entry point of the same
+name in libgbsort.so; all sorting work runs in that library's kernels.  The
+work buffer is a torch uint8 tensor that the caller may pass in and reuse
+(it is allocated here, never inside the library).
+
+The library is loaded on first use; if it is missing the call raises, so no
+computation can silently happen elsewhere.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgbsort.so")
+
+GBS_OK, GBS_ERR_INVALID_ARG, GBS_ERR_TEMP_TOO_SMALL, GBS_ERR_UNSUPPORTED, GBS_ERR_CUDA, GBS_ERR_TIMEOUT = range(6)
+GBS_U32, GBS_I32, GBS_F32, GBS_U64 = range(4)
+GBS_MAX_RADIX_KEYS = (1 << 29) - 1
+GBS_MAX_SEGMENT_LEN = 16384
+
+_DTYPE_KIND = {
+    torch.uint32: GBS_U32,
+    torch.int32: GBS_I32,
+    torch.float32: GBS_F32,
+    torch.uint64: GBS_U64,
+}
+_KIND_BYTES = {GBS_U32: 4, GBS_I32: 4, GBS_F32: 4, GBS_U64: 8}
+
+# every symbol the headers declare
+EXPORTS = ("gbs_sort_keys", "gbs_sort_pairs", "gbs_segmented_sort", "gbs_digit_histograms", "gbs_get_status",
+           "gbs_status_string", "gbs_version", "gbs_debug_set_lookback_fault", "gbs_debug_last_launch_count",
+           "gbs_debug_radix_tile_keys", "gbs_debug_set_timing_events")
+
+
+class GbsError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)}")
+        self.status = status
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Loads libgbsort.so (built by sorting_lsd_radix_gb300.build) and declares the prototypes."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"gbsort CUDA library not built: {p} is missing (run __graft_entry__.build())")
+    lib = ctypes.CDLL(p)
+    vp, sz, i, u32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_uint32
+    szp = ctypes.POINTER(ctypes.c_size_t)
+    lib.gbs_sort_keys.argtypes = [vp, szp, i, vp, vp, sz, i, i, i, vp]
+    lib.gbs_sort_keys.restype = i
+    lib.gbs_sort_pairs.argtypes = [vp, szp, i, vp, vp, vp, vp, sz, i, i, i, vp]
+    lib.gbs_sort_pairs.restype = i
+    lib.gbs_segmented_sort.argtypes = [vp, szp, i, vp, vp, sz, sz, i, vp]
+    lib.gbs_segmented_sort.restype = i
+    lib.gbs_digit_histograms.argtypes = [vp, szp, i, vp, sz, i, i, i, vp, vp]
+    lib.gbs_digit_histograms.restype = i
+    lib.gbs_get_status.argtypes = [vp, sz, vp]
+    lib.gbs_get_status.restype = i
+    lib.gbs_status_string.argtypes = [i]
+    lib.gbs_status_string.restype = ctypes.c_char_p
+    lib.gbs_version.argtypes = []
+    lib.gbs_version.restype = ctypes.c_char_p
+    lib.gbs_debug_set_lookback_fault.argtypes = [i, u32, u32]
+    lib.gbs_debug_set_lookback_fault.restype = None
+    lib.gbs_debug_last_launch_count.argtypes = []
+    lib.gbs_debug_last_launch_count.restype = i
+    lib.gbs_debug_radix_tile_keys.argtypes = [i, i]
+    lib.gbs_debug_radix_tile_keys.restype = sz
+    lib.gbs_debug_set_timing_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i]
+    lib.gbs_debug_set_timing_events.restype = None
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().gbs_status_string(status).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+def gbs_version() -> str:
+    return load().gbs_version().decode()
+
+
+def _kind(t: torch.Tensor, key_type: int | None) -> int:
+    if key_type is not None:
+        if _KIND_BYTES[key_type] != t.element_size():
+            raise ValueError("key_type does not match the tensor's element size")
+        return key_type
+    try:
+        return _DTYPE_KIND[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported key dtype {t.dtype}; pass key_type for a reinterpreting view") from None
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t: torch.Tensor | None) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr() if t is not None and t.numel() else 0)
+
+
+def _check_tensor(t: torch.Tensor, n: int, what: str):
+    if not t.is_cuda:
+        raise ValueError(f"{what} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+    if t.numel() != n:
+        raise ValueError(f"{what} must hold {n} elements")
+
+
+def _run(fn, args_after_temp, temp: torch.Tensor | None, what: str) -> torch.Tensor:
+    """Work-buffer protocol: query the size, (re)allocate with torch if needed, then run."""
+    need = ctypes.c_size_t(0)
+    st = fn(None, ctypes.byref(need), *args_after_temp)
+    if st != GBS_OK:
+        raise GbsError(st, what)
+    if temp is None or temp.numel() < need.value:
+        temp = torch.empty(max(need.value, 256), dtype=torch.uint8, device="cuda")
+    have = ctypes.c_size_t(temp.numel())
+    st = fn(_ptr(temp), ctypes.byref(have), *args_after_temp)
+    if st != GBS_OK:
+        raise GbsError(st, what)
+    return temp
+
+
+def temp_bytes(fn_name: str, *args) -> int:
+    """Work-buffer size a call with these C-level arguments needs (no launch)."""
+    need = ctypes.c_size_t(0)
+    st = getattr(load(), fn_name)(None, ctypes.byref(need), *args)
+    if st != GBS_OK:
+        raise GbsError(st, fn_name)
+    return need.value
+
+
+def gbs_sort_keys(keys_in: torch.Tensor, keys_out: torch.Tensor | None = None, begin_bit: int = 0,
+                  end_bit: int | None = None, descending: bool = False, temp: torch.Tensor | None = None,
+                  key_type: int | None = None, stream=None, return_temp: bool = False):
+    """Stable LSD radix sort of a CUDA tensor of keys by bits [begin_bit, end_bit) of their code.
+
+    keys_out may be keys_in (in place); None allocates a new tensor."""
+    kind = _kind(keys_in, key_type)
+    n = keys_in.numel()
+    _check_tensor(keys_in, n, "keys_in")
+    if keys_out is None:
+        keys_out = torch.empty_like(keys_in)
+    _check_tensor(keys_out, n, "keys_out")
+    if end_bit is None:
+        end_bit = 8 * _KIND_BYTES[kind]
+    args = (kind, _ptr(keys_in), _ptr(keys_out), n, begin_bit, end_bit, int(bool(descending)), _stream(stream))
+    temp = _run(load().gbs_sort_keys, args, temp, "gbs_sort_keys")
+    return (keys_out, temp) if return_temp else keys_out
+
+
+def gbs_sort_pairs(keys_in: torch.Tensor, vals_in: torch.Tensor, keys_out: torch.Tensor | None = None,
+                   vals_out: torch.Tensor | None = None, begin_bit: int = 0, end_bit: int | None = None,
+                   descending: bool = False, temp: torch.Tensor | None = None, key_type: int | None = None,
+                   stream=None, return_temp: bool = False):
+    """Stable LSD radix sort of (key, uint32 value) pairs; returns (keys_out, vals_out)."""
+    kind = _kind(keys_in, key_type)
+    n = keys_in.numel()
+    _check_tensor(keys_in, n, "keys_in")
+    _check_tensor(vals_in, n, "vals_in")
+    if vals_in.element_size() != 4:
+        raise ValueError("values must be 4-byte elements")
+    if keys_out is None:
+        keys_out = torch.empty_like(keys_in)
+    if vals_out is None:
+        vals_out = torch.empty_like(vals_in)
+    _check_tensor(keys_out, n, "keys_out")
+    _check_tensor(vals_out, n, "vals_out")
+    if end_bit is None:
+        end_bit = 8 * _KIND_BYTES[kind]
+    args = (kind, _ptr(keys_in), _ptr(keys_out), _ptr(vals_in), _ptr(vals_out), n, begin_bit, end_bit,
+            int(bool(descending)), _stream(stream))
+    temp = _run(load().gbs_sort_pairs, args, temp, "gbs_sort_pairs")
+    return (keys_out, vals_out, temp) if return_temp else (keys_out, vals_out)
+
+
+def gbs_segmented_sort(keys_in: torch.Tensor, num_segments: int, segment_len: int,
+                       keys_out: torch.Tensor | None = None, descending: bool = False,
+                       temp: torch.Tensor | None = None, key_type: int | None = None, stream=None):
+    """Bitonic sort of each of num_segments consecutive segments of segment_len keys."""
+    kind = _kind(keys_in, key_type)
+    n = num_segments * segment_len
+    _check_tensor(keys_in, n, "keys_in")
+    if keys_out is None:
+        keys_out = torch.empty_like(keys_in)
+    _check_tensor(keys_out, n, "keys_out")
+    args = (kind, _ptr(keys_in), _ptr(keys_out), num_segments, segment_len, int(bool(descending)), _stream(stream))
+    _run(load().gbs_segmented_sort, args, temp, "gbs_segmented_sort")
+    return keys_out
+
+
+def gbs_digit_histograms(keys: torch.Tensor, begin_bit: int = 0, end_bit: int | None = None,
+                         descending: bool = False, temp: torch.Tensor | None = None,
+                         key_type: int | None = None, stream=None) -> torch.Tensor:
+    """[passes, 256] uint32 digit counts computed by the upfront-histogram kernel."""
+    kind = _kind(keys, key_type)
+    n = keys.numel()
+    _check_tensor(keys, n, "keys")
+    if end_bit is None:
+        end_bit = 8 * _KIND_BYTES[kind]
+    passes = (end_bit - begin_bit + 7) // 8
+    hist = torch.zeros((max(passes, 1), 256), dtype=torch.int32, device="cuda")
+    args = (kind, _ptr(keys), n, begin_bit, end_bit, int(bool(descending)), _ptr(hist), _stream(stream))
+    _run(load().gbs_digit_histograms, args, temp, "gbs_digit_histograms")
+    return hist[:passes]
+
+
+def gbs_get_status(temp: torch.Tensor, stream=None) -> int:
+    """Synchronises the stream; GBS_ERR_TIMEOUT if the last call on this work buffer timed out."""
+    return load().gbs_get_status(_ptr(temp), temp.numel(), _stream(stream))
+
+
+def gbs_debug_set_lookback_fault(pass_index: int, tile: int, spin_limit: int) -> None:
+    load().gbs_debug_set_lookback_fault(pass_index, tile, spin_limit)
+
+
+def gbs_debug_last_launch_count() -> int:
+    return load().gbs_debug_last_launch_count()
+
+
+_timing_keepalive = None
+
+
+def gbs_debug_set_timing_events(events) -> None:
+    """events: list of torch.cuda.Event(enable_timing=True), or None to switch the hook off."""
+    global _timing_keepalive
+    if not events:
+        _timing_keepalive = None
+        load().gbs_debug_set_timing_events(None, 0)
+        return
+    arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _timing_keepalive = (arr, list(events))
+    load().gbs_debug_set_timing_events(arr, len(events))
+
+
+def gbs_debug_radix_tile_keys(key_bytes: int, pairs: bool = False) -> int:
+    return load().gbs_debug_radix_tile_keys(key_bytes, int(bool(pairs)))

@@ -1,0 +1,104 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads and
+exports every symbol the headers declare; argument checks and the work-buffer
+size query return the documented status codes without launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sorting_lsd_radix_gb300 import build as gbuild
+from sorting_lsd_radix_gb300 import gbsort
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gbsort.load()
+
+
+def _declared_functions():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(gbs_\w+)\s*\(", text):
+            names.add(m.group(1))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_functions()
+    assert {"gbs_sort_keys", "gbs_sort_pairs", "gbs_segmented_sort", "gbs_get_status"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert declared == set(gbsort.EXPORTS)
+
+
+def test_version_and_status_strings(lib):
+    assert gbsort.gbs_version() == "0.1.0"
+    assert gbsort.status_string(gbsort.GBS_ERR_TEMP_TOO_SMALL) == "GBS_ERR_TEMP_TOO_SMALL"
+    assert gbsort.status_string(99) == "GBS_ERR_UNKNOWN"
+
+
+def _query(lib, fn, *args):
+    need = ctypes.c_size_t(0)
+    st = getattr(lib, fn)(None, ctypes.byref(need), *args)
+    return st, need.value
+
+
+def test_temp_query_sizes(lib):
+    n = 10**6
+    st, need = _query(lib, "gbs_sort_keys", gbsort.GBS_U32, None, None, n, 0, 32, 0, None)
+    assert st == gbsort.GBS_OK
+    tile = gbsort.gbs_debug_radix_tile_keys(4)
+    tiles = (n + tile - 1) // tile
+    # header + 2 histogram blocks + status words + one scratch copy of the keys
+    assert need >= 256 + 2 * 8 * 256 * 4 + tiles * 1024 + 4 * n
+    assert need < 256 + 2 * 8 * 256 * 4 + tiles * 1024 + 4 * n + 4 * 256
+    st2, need2 = _query(lib, "gbs_sort_pairs", gbsort.GBS_U64, None, None, None, None, n, 0, 64, 0, None)
+    assert st2 == gbsort.GBS_OK and need2 >= 8 * n + 4 * n
+    st3, need3 = _query(lib, "gbs_segmented_sort", gbsort.GBS_U32, None, None, 16, 1024, 0, None)
+    assert st3 == gbsort.GBS_OK and need3 == 256
+
+
+@pytest.mark.parametrize("begin,end", [(-1, 8), (9, 8), (0, 33)])
+def test_bad_bit_range(lib, begin, end):
+    st, _ = _query(lib, "gbs_sort_keys", gbsort.GBS_U32, None, None, 10, begin, end, 0, None)
+    assert st == gbsort.GBS_ERR_INVALID_ARG
+
+
+def test_bad_key_type_and_limits(lib):
+    assert _query(lib, "gbs_sort_keys", 7, None, None, 10, 0, 8, 0, None)[0] == gbsort.GBS_ERR_INVALID_ARG
+    assert _query(lib, "gbs_sort_keys", gbsort.GBS_U32, None, None, gbsort.GBS_MAX_RADIX_KEYS + 1, 0, 32, 0,
+                  None)[0] == gbsort.GBS_ERR_UNSUPPORTED
+    assert _query(lib, "gbs_segmented_sort", gbsort.GBS_U32, None, None, 4, 16385, 0, None)[0] == \
+        gbsort.GBS_ERR_UNSUPPORTED
+    assert lib.gbs_sort_keys(None, None, gbsort.GBS_U32, None, None, 10, 0, 32, 0, None) == \
+        gbsort.GBS_ERR_INVALID_ARG
+
+
+def test_temp_too_small_and_misaligned(lib):
+    fake = ctypes.c_void_p(1 << 40)  # never dereferenced: the checks fail first
+    have = ctypes.c_size_t(100)
+    assert lib.gbs_sort_keys(fake, ctypes.byref(have), gbsort.GBS_U32, fake, fake, 1000, 0, 32, 0, None) == \
+        gbsort.GBS_ERR_TEMP_TOO_SMALL
+    big = ctypes.c_size_t(1 << 30)
+    odd = ctypes.c_void_p((1 << 40) + 16)
+    assert lib.gbs_sort_keys(odd, ctypes.byref(big), gbsort.GBS_U32, fake, fake, 1000, 0, 32, 0, None) == \
+        gbsort.GBS_ERR_INVALID_ARG
+
+
+def test_oracle_and_library_share_nothing():
+    # the oracle and the CUDA sources never include or import each other
+    csrc = os.path.join(ROOT, "sorting_lsd_radix_gb300", "csrc")
+    for f in os.listdir(csrc):
+        assert "oracle" not in open(os.path.join(csrc, f)).read().lower(), f
+    for f in ("oracle.c", "oracle.h", "__init__.py"):
+        text = open(os.path.join(ROOT, "oracle", f)).read()
+        assert "gbsort" not in text and "sorting_lsd_radix_gb300" not in text and "csrc" not in text, f
+    for f in ("gbsort.py", "build.py", "__init__.py"):
+        text = open(os.path.join(ROOT, "sorting_lsd_radix_gb300", f)).read()
+        assert "import oracle" not in text and "from oracle" not in text, f

@@ -1,0 +1,226 @@
+"""GPU parity: every entry point, through the C ABI, bit-exact against the oracle
+on the same seeded inputs (keys compared as bit patterns, values exactly)."""
+import numpy as np
+import pytest
+
+import oracle
+from sorting_lsd_radix_gb300 import workloads as wl
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+DTYPES = [np.uint32, np.int32, np.float32, np.uint64]
+
+
+@pytest.fixture(scope="module")
+def g():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sorting_lsd_radix_gb300 import build as gbuild
+    gbuild.build()
+    from sorting_lsd_radix_gb300 import gbsort
+    gbsort.load()
+    return gbsort
+
+
+def _u(a):
+    return a.view(np.uint64 if a.dtype.itemsize == 8 else np.uint32)
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _host(t):
+    return t.cpu().numpy()
+
+
+def sample(dtype, n, seed):
+    s = wl.seed_for(70, seed)
+    if dtype == np.uint32:
+        return wl.uniform_u32(n, s)
+    if dtype == np.int32:
+        return wl.uniform_i32(n, s)
+    if dtype == np.float32:
+        return wl.normal_mix_f32(n, s)
+    return wl.uniform_u64(n, s)
+
+
+def with_ties(dtype, n, seed, k=37):
+    base = sample(dtype, k, seed + 1000)
+    return base[(wl.uniform_u32(n, wl.seed_for(71, seed)) % np.uint32(k)).astype(np.int64)]
+
+
+TILE32 = 8192
+SIZES = [0, 1, 2, 31, 32, 33, 1023, 4095, 4096, 4097, TILE32 - 1, TILE32, TILE32 + 1, 16383, 16384, 16385,
+         3 * TILE32 + 5, (1 << 16) + 7, (1 << 20) + 3]
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("desc", [False, True])
+@pytest.mark.parametrize("n", SIZES)
+def test_sort_keys_full_range(g, dtype, desc, n):
+    keys = sample(dtype, n, n)
+    got = _host(g.gbs_sort_keys(_dev(keys), descending=desc))
+    assert np.array_equal(_u(got), _u(oracle.sort_keys(keys, descending=desc)))
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("desc", [False, True])
+@pytest.mark.parametrize("n", [3, 1000, 16384, 16385, 50001])
+def test_sort_pairs_with_ties_stable(g, dtype, desc, n):
+    keys = with_ties(dtype, n, n)
+    vals = np.arange(n, dtype=np.uint32)
+    ko, vo = g.gbs_sort_pairs(_dev(keys), _dev(vals), descending=desc)
+    ek, ev = oracle.sort_pairs(keys, vals, descending=desc)
+    assert np.array_equal(_u(_host(ko)), _u(ek))
+    assert np.array_equal(_host(vo), ev)
+
+
+BIT_RANGES = {np.uint32: [(0, 16), (3, 29), (8, 9), (0, 1), (31, 32), (5, 5), (16, 32), (0, 24)],
+              np.int32: [(0, 16), (20, 32)],
+              np.float32: [(0, 8), (23, 32)],
+              np.uint64: [(0, 52), (17, 64), (60, 64), (0, 8), (32, 64), (7, 7)]}
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("desc", [False, True])
+def test_partial_bit_ranges_pairs(g, dtype, desc):
+    n = 3 * TILE32 + 11
+    keys = sample(dtype, n, 5)
+    vals = np.arange(n, dtype=np.uint32)
+    for b, e in BIT_RANGES[dtype]:
+        ko, vo = g.gbs_sort_pairs(_dev(keys), _dev(vals), begin_bit=b, end_bit=e, descending=desc)
+        ek, ev = oracle.sort_pairs(keys, vals, b, e, descending=desc)
+        assert np.array_equal(_u(_host(ko)), _u(ek)), (b, e)
+        assert np.array_equal(_host(vo), ev), (b, e)
+        kk = g.gbs_sort_keys(_dev(keys), begin_bit=b, end_bit=e, descending=desc)
+        assert np.array_equal(_u(_host(kk)), _u(ek)), (b, e)
+
+
+@pytest.mark.parametrize("dist", list(wl.DISTRIBUTIONS_U32))
+@pytest.mark.parametrize("desc", [False, True])
+def test_distributions_u32(g, dist, desc):
+    n = (1 << 20) + 77
+    keys = wl.DISTRIBUTIONS_U32[dist](n, wl.seed_for(2, 3))
+    got = _host(g.gbs_sort_keys(_dev(keys), descending=desc))
+    assert np.array_equal(got, oracle.sort_keys(keys, descending=desc))
+    vals = np.arange(n, dtype=np.uint32)
+    ko, vo = g.gbs_sort_pairs(_dev(keys), _dev(vals), 0, 16, descending=desc)
+    ek, ev = oracle.sort_pairs(keys, vals, 0, 16, descending=desc)
+    assert np.array_equal(_host(ko), ek) and np.array_equal(_host(vo), ev)
+
+
+@pytest.mark.parametrize("dtype", [np.uint32, np.uint64])
+@pytest.mark.parametrize("n", [5000, 3 * TILE32 + 1, 200003])
+@pytest.mark.parametrize("bits", [(0, 32), (0, 8), (4, 20), (9, 9)])
+def test_in_place(g, dtype, n, bits):
+    keys = with_ties(dtype, n, 7, k=300) if dtype == np.uint32 else sample(dtype, n, 7) & np.uint64(0xFFFF00FF)
+    vals = np.arange(n, dtype=np.uint32)
+    tk, tv = _dev(keys), _dev(vals)
+    g.gbs_sort_pairs(tk, tv, keys_out=tk, vals_out=tv, begin_bit=bits[0], end_bit=bits[1])
+    ek, ev = oracle.sort_pairs(keys, vals, bits[0], bits[1])
+    assert np.array_equal(_host(tk), ek) and np.array_equal(_host(tv), ev)
+    tk2 = _dev(keys)
+    g.gbs_sort_keys(tk2, keys_out=tk2, begin_bit=bits[0], end_bit=bits[1], descending=True)
+    assert np.array_equal(_host(tk2), oracle.sort_keys(keys, bits[0], bits[1], descending=True))
+
+
+def test_all_passes_trivial_and_skipped_passes(g):
+    n = 3 * TILE32 + 9
+    eq = wl.all_equal_u32(n, 1)
+    assert np.array_equal(_host(g.gbs_sort_keys(_dev(eq), begin_bit=0, end_bit=32)), eq)
+    vals = np.arange(n, dtype=np.uint32)
+    ko, vo = g.gbs_sort_pairs(_dev(eq), _dev(vals))
+    assert np.array_equal(_host(vo), vals)
+    # only the middle byte varies: passes 0, 1 and 3 are trivial
+    k = (wl.uniform_u32(n, 2) & np.uint32(0x00FF0000)) | np.uint32(0x12003456)
+    ko, vo = g.gbs_sort_pairs(_dev(k), _dev(vals))
+    assert g.gbs_debug_last_launch_count() == 5  # histogram + four pass kernels
+    ek, ev = oracle.sort_pairs(k, vals)
+    assert np.array_equal(_host(ko), ek) and np.array_equal(_host(vo), ev)
+    # u64 keys whose top byte is zero (7 active passes of 8)
+    k64 = wl.priority_u64(n, 3)
+    ko, vo = g.gbs_sort_pairs(_dev(k64), _dev(vals))
+    ek, ev = oracle.sort_pairs(k64, vals)
+    assert np.array_equal(_host(ko), ek) and np.array_equal(_host(vo), ev)
+
+
+def test_unaligned_pointers_use_plain_loads(g):
+    n = 5 * TILE32 + 3
+    base = wl.uniform_u32(n + 1, 9)
+    t = _dev(base)
+    view_in = t[1:]  # 4-byte aligned, not 16-byte aligned
+    out = torch.empty(n + 1, dtype=torch.uint32, device="cuda")[1:]
+    g.gbs_sort_keys(view_in, keys_out=out, begin_bit=0, end_bit=24)
+    assert np.array_equal(_host(out), oracle.sort_keys(base[1:], 0, 24))
+
+
+def test_temp_reuse_across_calls(g):
+    n = 100000
+    a = wl.uniform_u32(n, 11)
+    b = wl.low_entropy_u32(n, 12)
+    _, temp = g.gbs_sort_keys(_dev(a), return_temp=True, begin_bit=0, end_bit=20)
+    for keys in (b, a, b):
+        got = _host(g.gbs_sort_keys(_dev(keys), temp=temp, begin_bit=0, end_bit=20))
+        assert np.array_equal(got, oracle.sort_keys(keys, 0, 20))
+    assert g.gbs_get_status(temp) == g.GBS_OK
+
+
+SEG_LENS = [1, 2, 3, 5, 16, 31, 32, 33, 100, 255, 256, 1000, 1024, 1025, 2048, 4096, 8191, 8192, 16383, 16384]
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("seg_len", SEG_LENS)
+def test_segmented_sort(g, dtype, seg_len):
+    segs = max(3, min(300, (1 << 18) // seg_len))
+    keys = sample(dtype, segs * seg_len, seg_len)
+    if seg_len % 3 == 0:
+        keys = with_ties(dtype, segs * seg_len, seg_len)
+    for desc in (False, True):
+        got = _host(g.gbs_segmented_sort(_dev(keys), segs, seg_len, descending=desc))
+        assert np.array_equal(_u(got), _u(oracle.segmented_sort(keys, segs, seg_len, descending=desc))), desc
+
+
+def test_segmented_zero_one_principle_exhaustive(g):
+    # every 0-1 pattern of 16 keys, one per segment ("并行排序" §1.2, 0-1 principle)
+    pats = wl.zero_one_patterns(16)
+    got = _host(g.gbs_segmented_sort(_dev(pats.reshape(-1)), pats.shape[0], 16)).reshape(pats.shape)
+    ones = pats.sum(axis=1)
+    want = (np.arange(16)[None, :] >= (16 - ones)[:, None]).astype(np.uint32)
+    assert np.array_equal(got, want)
+    assert np.array_equal(got.reshape(-1), oracle.segmented_sort(pats.reshape(-1), pats.shape[0], 16))
+
+
+def test_segmented_in_place_and_empty(g):
+    keys = sample(np.uint32, 64 * 700, 3)
+    t = _dev(keys)
+    g.gbs_segmented_sort(t, 64, 700, keys_out=t, descending=True)
+    assert np.array_equal(_host(t), oracle.segmented_sort(keys, 64, 700, descending=True))
+    e = torch.empty(0, dtype=torch.uint32, device="cuda")
+    assert g.gbs_segmented_sort(e, 0, 100).numel() == 0
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("desc", [False, True])
+def test_digit_histograms(g, dtype, desc):
+    n = 200001
+    keys = with_ties(dtype, n, 4) if dtype == np.float32 else sample(dtype, n, 4)
+    for b, e in [(0, 8 * keys.dtype.itemsize), (3, 29), (0, 16)]:
+        got = _host(g.gbs_digit_histograms(_dev(keys), b, e, descending=desc)).astype(np.int64)
+        assert np.array_equal(got, oracle.digit_histograms(keys, b, e, descending=desc).astype(np.int64))
+
+
+def test_worked_example_on_gpu(g):
+    src = np.array([4, 2, 7, 1, 8, 3, 6, 5], dtype=np.uint32)  # kwkr.cn notes §2.2
+    assert _host(g.gbs_sort_keys(_dev(src))).tolist() == [1, 2, 3, 4, 5, 6, 7, 8]
+    assert _host(g.gbs_segmented_sort(_dev(src), 1, 8)).tolist() == [1, 2, 3, 4, 5, 6, 7, 8]
+
+
+def test_float_special_values(g):
+    vals = np.array([np.inf, -0.0, 0.0, -np.inf, 1.0, -1.0, np.float32(1e-45), -np.float32(1e-45), 3.4e38,
+                     -3.4e38] * 3000, dtype=np.float32)
+    for desc in (False, True):
+        for n in (30, 30000):
+            got = _host(g.gbs_sort_keys(_dev(vals[:n]), descending=desc))
+            assert np.array_equal(got.view(np.uint32), oracle.sort_keys(vals[:n], descending=desc).view(np.uint32))
