@@ -35,13 +35,13 @@ UNIT = "keys/s"
 WORKLOAD = "sort_keys u32 ascending, bits [0,32), n=1e8 i.i.d. uniform keys (SplitMix64)"
 FALLBACK_HBM_GBS = 6800.0
 PASS_KERNEL_SOURCES = ["sorting_lsd_radix_gb300/csrc/radix.cu", "sorting_lsd_radix_gb300/csrc/common.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "onesweep_pass_u32_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "onesweep_pass_u32_2p26.md")
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gbsort", choices=["gbsort", "reference"])
     ap.add_argument("--n", type=int, default=N_KEYS)
@@ -69,16 +69,24 @@ def source_hash():
 
 
 def recorded_traffic(n):
-    """DRAM bytes per pass-kernel launch from the committed ncu summary, scaled to n keys;
-    None if absent or taken on a different kernel source."""
+    """DRAM bytes per pass-kernel launch from the committed ncu summary, scaled to n keys
+    (traffic grows in proportion to n); None if absent or taken on a different kernel source."""
     try:
-        with open(TRAFFIC_FILE) as f:
-            d = json.load(f)
-    except Exception:
+        lines = open(TRAFFIC_FILE).read().splitlines()
+    except OSError:
         return None
-    if d.get("source_hash") != source_hash():
+    rec = {}
+    for ln in lines:
+        if ":" in ln:
+            k, v = ln.split(":", 1)
+            rec[k.strip()] = v.split()
+    try:
+        if rec["source_sha256_16"][0] != source_hash():
+            return None
+        n_cap, bytes_cap = (float(x) for x in rec["traffic_bytes_per_launch_at_n"][:2])
+    except (KeyError, ValueError, IndexError):
         return None
-    return float(d["dram_bytes_per_launch"]) * n / float(d["n"])
+    return bytes_cap * n / n_cap
 
 
 class ClockSampler:
@@ -92,7 +100,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
 
@@ -206,6 +214,9 @@ def run_gbsort(args):
         gbsort.gbs_sort_keys(d_in, d_out, temp=temp)
     # per-kernel events for every timed step (histogram, 4 passes)
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(launches + 1)] for _ in range(args.steps)]
+    for evs in events:  # torch creates the CUDA event on first record
+        for e in evs:
+            e.record(stream)
     barrier()
     sampler = ClockSampler(local)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -280,7 +291,8 @@ def run_gbsort(args):
                    "parallelism": f"{world} independent sorts (one per GPU)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "onesweep_pass_kernel<u32,keys,512x16>", "peak_kind": f"{peak_kind} hbm_gbs",
+                     "kernel": f"onesweep_pass_kernel<u32,keys,tile={gbsort.gbs_debug_radix_tile_keys(4)}>",
+                     "peak_kind": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": alg_pass, "avg_launch_ms": pass_ms},
         "whole_sort": {"achieved_gbs": alg_total / (ms_per_step / 1e3) / 1e9,
                        "frac_of_peak": alg_total / (ms_per_step / 1e3) / 1e9 / peak,

@@ -37,7 +37,9 @@ thread_local int t_event_next = 0;
 // Records events[0] before a call's first kernel (see gbs_debug_set_timing_events).
 void timing_start(cudaStream_t s) {
     t_event_next = 0;
-    if (t_events && t_event_count > 0) cudaEventRecord(reinterpret_cast<cudaEvent_t>(t_events[t_event_next++]), s);
+    if (t_events && t_event_count > 0 &&
+        cudaEventRecord(reinterpret_cast<cudaEvent_t>(t_events[t_event_next++]), s) != cudaSuccess)
+        (void)cudaGetLastError();  // a bad caller event must not be reported as a launch failure
 }
 
 // Work-buffer layout of a radix call.
@@ -150,8 +152,9 @@ gbs_status radix_common(void *d_temp, size_t *temp_bytes, gbs_key_type kt, const
 
 namespace gbs {
 void timing_mark(cudaStream_t s) {
-    if (t_events && t_event_next > 0 && t_event_next < t_event_count)
-        cudaEventRecord(reinterpret_cast<cudaEvent_t>(t_events[t_event_next++]), s);
+    if (t_events && t_event_next > 0 && t_event_next < t_event_count &&
+        cudaEventRecord(reinterpret_cast<cudaEvent_t>(t_events[t_event_next++]), s) != cudaSuccess)
+        (void)cudaGetLastError();
 }
 }  // namespace gbs
 

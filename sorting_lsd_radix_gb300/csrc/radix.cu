@@ -44,6 +44,41 @@ __device__ __forceinline__ uint32_t excl_scan_256(uint32_t v, uint32_t *wsum) {
 }
 
 // ---------------------------------------------------------------------------
+// Peer mask: the lanes of the (fully active) warp whose 8-bit digit equals
+// this lane's.  One ballot per digit bit gives the warp's eight bit planes.
+// Lane l then builds the peer mask of the nibble value l & 15 — over planes
+// 0..3 for lanes 0..15 (low nibble) and planes 4..7 for lanes 16..31 (high
+// nibble) — and every lane fetches the masks of its own two nibbles with two
+// shuffles; their AND is the peer mask.  Must be called by all 32 lanes.
+// ---------------------------------------------------------------------------
+struct NibbleLane {
+    uint32_t s0, s1, s2, s3;  // all ones where bit k of (lane & 15) is set
+    bool high;
+    __device__ __forceinline__ explicit NibbleLane(int lane) {
+        const uint32_t v = (uint32_t)lane & 15u;
+        s0 = 0u - (v & 1u);
+        s1 = 0u - ((v >> 1) & 1u);
+        s2 = 0u - ((v >> 2) & 1u);
+        s3 = 0u - ((v >> 3) & 1u);
+        high = lane >= 16;
+    }
+};
+
+__device__ __forceinline__ void warp_peer_halves(uint32_t d, const NibbleLane &nl, uint32_t &e_lo,
+                                                 uint32_t &e_hi) {
+    uint32_t b[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) b[k] = __ballot_sync(FULL, (d >> k) & 1u);
+    const uint32_t p0 = nl.high ? b[4] : b[0];
+    const uint32_t p1 = nl.high ? b[5] : b[1];
+    const uint32_t p2 = nl.high ? b[6] : b[2];
+    const uint32_t p3 = nl.high ? b[7] : b[3];
+    const uint32_t e = ~(p0 ^ nl.s0) & ~(p1 ^ nl.s1) & ~(p2 ^ nl.s2) & ~(p3 ^ nl.s3);
+    e_lo = __shfl_sync(FULL, e, (int)(d & 15u));         // lanes agreeing on the low nibble
+    e_hi = __shfl_sync(FULL, e, (int)(16u + (d >> 4)));  // ... and on the high nibble
+}
+
+// ---------------------------------------------------------------------------
 // Upfront histogram of all digit passes (one read of the keys)
 // ---------------------------------------------------------------------------
 
@@ -179,9 +214,10 @@ template <typename K, bool PAIRS, int THREADS, int ITEMS> struct PassSmem {
     static constexpr int WARPS = THREADS / 32;
     K keys[TILE];
     uint32_t vals[PAIRS ? TILE : 4];
-    uint32_t whist[WARPS][256];  // per-warp digit counts, then warp-exclusive offsets
-    uint32_t local[256];         // exclusive prefix of the tile's digit counts
-    uint32_t binoff[256];        // global position of sorted-tile slot 0 of each digit
+    // per-warp digit counters; after the count phase: sorted-tile slot of the
+    // warp's first key of each digit
+    uint32_t whist[WARPS][256];
+    uint32_t binoff[256];  // global position of sorted-tile slot 0 of each digit
     uint32_t wsum[8];
     uint32_t tile;
     alignas(8) uint64_t bar;
@@ -195,10 +231,13 @@ struct PassParams {
     uint32_t *vals_out;
     uint32_t *vals_alt;
     uint32_t n;
-    int kind;
+    // order-preserving code of a 32-bit key: x ^ ((x >>s 31) & enc_a) ^ enc_b;
+    // 64-bit keys: x ^ flip
+    uint32_t enc_a, enc_b;
     uint64_t flip;
     int pass, num_passes, shift;
     uint32_t mask;
+    uint32_t perm_sel;  // byte-permute selector of the digit byte (byte-aligned passes)
     int in_place;
     Header *hdr;
     const uint32_t *digit_base;
@@ -208,16 +247,168 @@ struct PassParams {
     uint32_t fault_tile;
 };
 
+template <typename K> struct Xform;
+template <> struct Xform<uint32_t> {
+    static __device__ __forceinline__ uint32_t enc(uint32_t x, const PassParams &p) {
+        return x ^ (((uint32_t)((int32_t)x >> 31) & p.enc_a) ^ p.enc_b);
+    }
+    static __device__ __forceinline__ uint32_t dec(uint32_t t, const PassParams &p) {
+        const uint32_t f = (uint32_t)p.flip;
+        const uint32_t u = t ^ f;  // code without the descending complement
+        return u ^ ((~(uint32_t)((int32_t)u >> 31) & p.enc_a) ^ (p.enc_b ^ f));
+    }
+};
+template <> struct Xform<uint64_t> {
+    static __device__ __forceinline__ uint64_t enc(uint64_t x, const PassParams &p) { return x ^ p.flip; }
+    static __device__ __forceinline__ uint64_t dec(uint64_t t, const PassParams &p) { return t ^ p.flip; }
+};
+
+// Digit of a code for this pass.  BYTE: the digit is a whole byte of the
+// code (begin_bit a multiple of 8 and an 8-bit digit), extracted with one
+// byte permute.
+template <bool BYTE> __device__ __forceinline__ uint32_t pass_digit(uint32_t t, const PassParams &p) {
+    return BYTE ? __byte_perm(t, 0u, p.perm_sel) : digit_of(t, p.shift, p.mask);
+}
+template <bool BYTE> __device__ __forceinline__ uint32_t pass_digit(uint64_t t, const PassParams &p) {
+    if (BYTE) {
+        const uint32_t w = p.shift >= 32 ? (uint32_t)(t >> 32) : (uint32_t)t;
+        return __byte_perm(w, 0u, p.perm_sel);
+    }
+    return digit_of(t, p.shift, p.mask);
+}
+
 template <typename K>
 __device__ __forceinline__ void copy_range(const K *src, K *dst, size_t lo, size_t hi, int tid, int nthreads) {
     for (size_t i = lo + tid; i < hi; i += nthreads) dst[i] = src[i];
 }
 
-template <typename K, bool PAIRS, int THREADS, int ITEMS>
-__global__ void __launch_bounds__(THREADS, 2) onesweep_pass_kernel(const PassParams prm) {
+// Stable warp rank of a full tile's keys (see the kernel); ENC applies the
+// key code on load (first active pass).  The highest lane of each digit group
+// adds the group size to the warp's counter with one shared-memory atomic and
+// hands the old value to its peers.
+// In-tile ranks are kept as 16-bit halves, two per register.
+template <int ITEMS> struct PackedRanks {
+    uint32_t r[(ITEMS + 1) / 2];
+    __device__ __forceinline__ void set(int i, uint32_t v) {
+        if (i & 1)
+            r[i >> 1] |= v << 16;
+        else
+            r[i >> 1] = v;
+    }
+    __device__ __forceinline__ void replace(int i, uint32_t v) {
+        if (i & 1)
+            r[i >> 1] = (r[i >> 1] & 0xFFFFu) | (v << 16);
+        else
+            r[i >> 1] = (r[i >> 1] & 0xFFFF0000u) | v;
+    }
+    __device__ __forceinline__ uint32_t get(int i) const { return (i & 1) ? (r[i >> 1] >> 16) : (r[i >> 1] & 0xFFFFu); }
+};
+
+// Stable warp rank.  Warp w owns tile slots [w*ITEMS*32, (w+1)*ITEMS*32);
+// item i of lane l is slot w*ITEMS*32 + 32 i + l, so (warp, item, lane) is
+// input order.  Lanes holding the same digit find each other (peer mask); the
+// highest of them advances the warp's counter for that digit by the group
+// size with one shared-memory atomic and hands the old value to its peers.
+// The peer masks of two consecutive items are formed before their counter
+// updates, which stay in item order.  ENC applies the key code on load
+// (first active pass).  Output: keys (coded) and their ranks within the warp's
+// digit groups; whist ends holding the warp's digit counts.
+template <bool ENC, bool BYTE, bool FULLTILE, typename K, int ITEMS>
+__device__ __forceinline__ void rank_warp(const K *tile_keys, uint32_t *whist, const PassParams &prm, int warp,
+                                          int lane, uint32_t valid, K (&keys)[ITEMS], PackedRanks<ITEMS> &ranks) {
+    const NibbleLane nl(lane);
+    const uint32_t lt = lanemask_lt();
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) {
+        const uint32_t idx = (uint32_t)warp * (ITEMS * 32) + i * 32 + lane;
+        K key = (FULLTILE || idx < valid) ? tile_keys[idx] : (K)0;
+        if (ENC) key = Xform<K>::enc(key, prm);
+        keys[i] = key;
+    }
+#pragma unroll
+    for (int i = 0; i < ITEMS; i += 2) {
+        uint32_t peers[2], d[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (i + u < ITEMS) {
+                d[u] = pass_digit<BYTE>(keys[i + u], prm);
+                uint32_t e_lo, e_hi;
+                warp_peer_halves(d[u], nl, e_lo, e_hi);
+                peers[u] = e_lo & e_hi;
+                if (!FULLTILE) {
+                    const uint32_t idx = (uint32_t)warp * (ITEMS * 32) + (i + u) * 32 + lane;
+                    const bool ok = idx < valid;
+                    const uint32_t vmask = __ballot_sync(FULL, ok);
+                    peers[u] &= ok ? vmask : 0u;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (i + u < ITEMS) {
+                const bool ok = FULLTILE || peers[u] != 0u;
+                const int leader = ok ? 31 - __clz(peers[u]) : lane;
+                uint32_t before = 0;
+                if (ok && lane == leader) before = atomicAdd(&whist[d[u]], (uint32_t)__popc(peers[u]));
+                const uint32_t b = __shfl_sync(FULL, before, leader);
+                ranks.set(i + u, ok ? b + __popc(peers[u] & lt) : 0u);
+            }
+        }
+    }
+}
+
+// Coalesced scatter of the sorted tile: consecutive slots of one digit go to
+// consecutive global positions.  DEC applies the inverse key code (last pass).
+template <bool DEC, bool BYTE, typename K, bool PAIRS, int THREADS>
+__device__ __forceinline__ void store_tile(const K *sk, const uint32_t *sv, const uint32_t *binoff, uint32_t valid,
+                                           K *kdst, uint32_t *vdst, const PassParams &prm, int tid) {
+#pragma unroll 4
+    for (uint32_t j = tid; j < valid; j += THREADS) {
+        const K key = sk[j];
+        const uint32_t pos = binoff[pass_digit<BYTE>(key, prm)] + j;
+        kdst[pos] = DEC ? Xform<K>::dec(key, prm) : key;
+        if (PAIRS) vdst[pos] = sv[j];
+    }
+}
+
+// Bounded wait for phase `parity` of the tile-load barrier; a copy that never
+// lands records ERR_COPY_TIMEOUT instead of hanging.
+__device__ __forceinline__ void wait_phase(uint64_t *bar, uint32_t parity, const PassParams &prm, Header *hdr,
+                                           uint32_t tile) {
+    uint32_t polls = 0;
+    while (!mbar_try_wait(bar, parity & 1u)) {
+        if (++polls > prm.spin_limit) {
+            record_error(hdr, ERR_COPY_TIMEOUT, ((uint32_t)prm.pass << 24) | (tile & 0xFFFFFFu));
+            break;
+        }
+        if (polls > 16) __nanosleep(64);
+    }
+}
+
+#ifndef LOOKBACK_WINDOW
+#define LOOKBACK_WINDOW 16
+#endif
+#ifndef GBS_PASS_MINB
+#define GBS_PASS_MINB 2
+#endif
+#ifndef GBS_U32_THREADS
+#define GBS_U32_THREADS 512
+#endif
+#ifndef GBS_U32_ITEMS
+#define GBS_U32_ITEMS 24
+#endif
+#ifndef GBS_U32_PAIR_ITEMS
+#define GBS_U32_PAIR_ITEMS 16
+#endif
+
+template <typename K, bool PAIRS, int THREADS, int ITEMS, bool BYTE>
+__global__ void __launch_bounds__(THREADS, GBS_PASS_MINB) onesweep_pass_kernel(const PassParams prm) {
+    static_assert(THREADS * ITEMS <= 65536, "in-tile ranks are 16-bit");
     using S = PassSmem<K, PAIRS, THREADS, ITEMS>;
     constexpr int TILE = S::TILE;
     constexpr int WARPS = S::WARPS;
+    // one thread per digit in the count, scan and look-back phases
+    static_assert(THREADS >= 256 && THREADS % 32 == 0, "the pass kernel needs at least 256 threads");
     extern __shared__ __align__(128) unsigned char smem_raw[];
     S &sm = *reinterpret_cast<S *>(smem_raw);
 
@@ -259,73 +450,76 @@ __global__ void __launch_bounds__(THREADS, 2) onesweep_pass_kernel(const PassPar
 
     // chained-scan states of this pass (rotated by ordinal, see common.cuh)
     const uint32_t st_agg = 1u + 2u * (k % 3u), st_inc = 2u + 2u * (k % 3u);
+    const bool aligned = ((reinterpret_cast<uintptr_t>(ksrc) & 15) == 0) &&
+                         (!PAIRS || ((reinterpret_cast<uintptr_t>(vsrc) & 15) == 0));
+    const uint32_t tx_bytes = TILE * (uint32_t)sizeof(K) + (PAIRS ? TILE * 4u : 0u);
 
+    // ---- ticket and tile load ---------------------------------------------
+    // Tiles are taken in ticket order (forward progress of the look-back).
+    // The ticket usually equals blockIdx.x, so that tile's bulk copy is issued
+    // before the ticket atomic returns; a different ticket waits for the
+    // speculative copy to land and loads its own tile.
+    const uint32_t spec = blockIdx.x;
+    const bool spec_ok = aligned && ((size_t)(spec + 1) * TILE <= (size_t)prm.n);
     if (tid == 0) {
-        sm.tile = atomicAdd(&hdr->tile_counter[prm.pass], 1u);
         mbar_init(&sm.bar, 1);
         fence_mbar_init();
+        if (spec_ok) {
+            mbar_arrive_expect_tx(&sm.bar, tx_bytes);
+            bulk_g2s(sm.keys, ksrc + (size_t)spec * TILE, TILE * (uint32_t)sizeof(K), &sm.bar);
+            if (PAIRS) bulk_g2s(sm.vals, vsrc + (size_t)spec * TILE, TILE * 4u, &sm.bar);
+        }
+        sm.tile = atomicAdd(&hdr->tile_counter[prm.pass], 1u);
     }
+    const uint32_t dbase = (tid < 256) ? prm.digit_base[prm.pass * 256 + tid] : 0u;
     for (int i = tid; i < WARPS * 256; i += THREADS) (&sm.whist[0][0])[i] = 0;
     __syncthreads();
     const uint32_t tile = sm.tile;
     const size_t tile_start = (size_t)tile * TILE;
     const uint32_t valid = (uint32_t)min((size_t)TILE, (size_t)prm.n - tile_start);
-
-    // ---- tile load: one bulk async copy per array, or plain loads --------
-    const K *gk = ksrc + tile_start;
-    const bool bulk = (valid == TILE) && ((reinterpret_cast<uintptr_t>(gk) & 15) == 0) &&
-                      (!PAIRS || ((reinterpret_cast<uintptr_t>(vsrc + tile_start) & 15) == 0));
-    if (bulk) {
-        if (tid == 0) {
-            mbar_arrive_expect_tx(&sm.bar,
-                                  TILE * (uint32_t)sizeof(K) + (PAIRS ? TILE * 4u : 0u));
-            bulk_g2s(sm.keys, gk, TILE * (uint32_t)sizeof(K), &sm.bar);
-            if (PAIRS) bulk_g2s(sm.vals, vsrc + tile_start, TILE * 4u, &sm.bar);
+    {
+        uint32_t phase = 0;
+        bool have = false;
+        if (spec_ok) {
+            wait_phase(&sm.bar, phase, prm, hdr, tile);  // the speculative copy has landed
+            ++phase;
+            have = (tile == spec);
         }
-        uint32_t polls = 0;
-        while (!mbar_try_wait(&sm.bar, 0)) {
-            if (++polls > prm.spin_limit) {
-                record_error(hdr, ERR_COPY_TIMEOUT, ((uint32_t)prm.pass << 24) | (tile & 0xFFFFFFu));
-                break;
+        if (!have) {
+            // every thread must have seen phase 0 complete before phase 1 can
+            // start, or a late poller of parity 0 would wait on phase 2
+            if (spec_ok) __syncthreads();
+            if (valid == TILE && aligned) {
+                if (tid == 0) {
+                    mbar_arrive_expect_tx(&sm.bar, tx_bytes);
+                    bulk_g2s(sm.keys, ksrc + tile_start, TILE * (uint32_t)sizeof(K), &sm.bar);
+                    if (PAIRS) bulk_g2s(sm.vals, vsrc + tile_start, TILE * 4u, &sm.bar);
+                }
+                wait_phase(&sm.bar, phase, prm, hdr, tile);
+            } else {
+                for (uint32_t i = tid; i < valid; i += THREADS) {
+                    sm.keys[i] = ksrc[tile_start + i];
+                    if (PAIRS) sm.vals[i] = vsrc[tile_start + i];
+                }
+                __syncthreads();
             }
-            if (polls > 16) __nanosleep(64);
         }
-    } else {
-        for (uint32_t i = tid; i < valid; i += THREADS) {
-            sm.keys[i] = gk[i];
-            if (PAIRS) sm.vals[i] = vsrc[tile_start + i];
-        }
-        __syncthreads();
     }
 
     // ---- stable rank within the tile --------------------------------------
-    // Warp w owns tile slots [w*ITEMS*32, (w+1)*ITEMS*32); item i of lane l is
-    // slot w*ITEMS*32 + 32 i + l, so (warp, item, lane) is input order.  Lanes
-    // holding the same digit find each other with match.any; the lowest of
-    // them advances the warp's counter for that digit by the group size.
-    const K flip = (K)prm.flip;
     K keys[ITEMS];
-    uint32_t ranks[ITEMS];
+    PackedRanks<ITEMS> ranks;
     uint32_t *whist = sm.whist[warp];
-    const uint32_t lt = lanemask_lt();
-#pragma unroll
-    for (int i = 0; i < ITEMS; ++i) {
-        const uint32_t idx = (uint32_t)warp * (ITEMS * 32) + i * 32 + lane;
-        const bool ok = idx < valid;
-        K key = ok ? sm.keys[idx] : (K)0;
-        if (first) key = KeyCodec<K>::enc(key, prm.kind, flip);
-        keys[i] = key;
-        const uint32_t d = digit_of(key, prm.shift, prm.mask);
-        const uint32_t vmask = __ballot_sync(FULL, ok);
-        ranks[i] = 0;
-        if (ok) {
-            const uint32_t peers = __match_any_sync(vmask, d);
-            const uint32_t before = whist[d];
-            __syncwarp(vmask);
-            if (lane == __ffs(peers) - 1) whist[d] = before + __popc(peers);
-            __syncwarp(vmask);
-            ranks[i] = before + __popc(peers & lt);
-        }
+    if (valid == TILE) {
+        if (first)
+            rank_warp<true, BYTE, true>(sm.keys, whist, prm, warp, lane, valid, keys, ranks);
+        else
+            rank_warp<false, BYTE, true>(sm.keys, whist, prm, warp, lane, valid, keys, ranks);
+    } else {
+        if (first)
+            rank_warp<true, BYTE, false>(sm.keys, whist, prm, warp, lane, valid, keys, ranks);
+        else
+            rank_warp<false, BYTE, false>(sm.keys, whist, prm, warp, lane, valid, keys, ranks);
     }
     __syncthreads();
 
@@ -345,33 +539,10 @@ __global__ void __launch_bounds__(THREADS, 2) onesweep_pass_kernel(const PassPar
         if (!faulty) st_relaxed_gpu(my_status + tid, ((tile == 0 ? st_inc : st_agg) << STATUS_COUNT_BITS) | run);
     }
     const uint32_t local = excl_scan_256(cnt, sm.wsum);
-
-    // ---- decoupled look-back over the predecessors' status words ----------
     if (tid < 256) {
-        uint32_t excl = 0;
-        if (tile > 0) {
-            uint32_t j = tile - 1;
-            uint32_t polls = 0;
-            for (;;) {
-                const uint32_t s = ld_relaxed_gpu(prm.status + (size_t)j * 256 + tid);
-                const uint32_t st = s >> STATUS_COUNT_BITS;
-                if (st == st_agg || st == st_inc) {
-                    excl += s & STATUS_COUNT_MASK;
-                    if (st == st_inc || j == 0) break;
-                    --j;
-                    continue;
-                }
-                if (++polls > prm.spin_limit) {
-                    record_error(hdr, ERR_LOOKBACK_TIMEOUT, ((uint32_t)prm.pass << 24) | (tile & 0xFFFFFFu));
-                    break;
-                }
-                __nanosleep(polls < 64 ? 32 : 256);
-            }
-            if (!faulty)
-                st_relaxed_gpu(my_status + tid, (st_inc << STATUS_COUNT_BITS) | ((excl + cnt) & STATUS_COUNT_MASK));
-        }
-        sm.local[tid] = local;
-        sm.binoff[tid] = prm.digit_base[prm.pass * 256 + tid] + excl - local;
+        // sorted-tile slot of each warp's first key of digit tid
+#pragma unroll 4
+        for (int w = 0; w < WARPS; ++w) sm.whist[w][tid] += local;
     }
     __syncthreads();
 
@@ -379,10 +550,10 @@ __global__ void __launch_bounds__(THREADS, 2) onesweep_pass_kernel(const PassPar
 #pragma unroll
     for (int i = 0; i < ITEMS; ++i) {
         const uint32_t idx = (uint32_t)warp * (ITEMS * 32) + i * 32 + lane;
-        if (idx < valid) {
-            const uint32_t d = digit_of(keys[i], prm.shift, prm.mask);
-            ranks[i] += sm.local[d] + whist[d];  // slot in the sorted tile
-            sm.keys[ranks[i]] = keys[i];
+        if (valid == TILE || idx < valid) {
+            const uint32_t slot = ranks.get(i) + whist[pass_digit<BYTE>(keys[i], prm)];
+            if (PAIRS) ranks.replace(i, slot);
+            sm.keys[slot] = keys[i];
         }
     }
     if (PAIRS) {
@@ -396,20 +567,60 @@ __global__ void __launch_bounds__(THREADS, 2) onesweep_pass_kernel(const PassPar
 #pragma unroll
         for (int i = 0; i < ITEMS; ++i) {
             const uint32_t idx = (uint32_t)warp * (ITEMS * 32) + i * 32 + lane;
-            if (idx < valid) sm.vals[ranks[i]] = vals[i];
+            if (idx < valid) sm.vals[ranks.get(i)] = vals[i];
         }
+    }
+
+    // ---- decoupled look-back over the predecessors' status words ----------
+    // Each digit's thread reads LOOKBACK_WINDOW predecessors per round trip
+    // (registers are free again: the tile's keys now sit in shared memory),
+    // adds the aggregates from the nearest one back to the first inclusive
+    // prefix, and waits (bounded) only at a predecessor that has published
+    // nothing yet.
+    if (tid < 256) {
+        uint32_t excl = 0;
+        if (tile > 0) {
+            int32_t lb_next = (int32_t)tile - 1;  // nearest predecessor not yet added
+            uint32_t polls = 0;
+            for (;;) {
+                uint32_t sw[LOOKBACK_WINDOW];
+#pragma unroll
+                for (int w = 0; w < LOOKBACK_WINDOW; ++w)
+                    sw[w] = (lb_next - w >= 0) ? ld_relaxed_gpu(prm.status + (size_t)(lb_next - w) * 256 + tid)
+                                               : (st_inc << STATUS_COUNT_BITS);
+                int used = 0;
+                bool done = false;
+#pragma unroll
+                for (int w = 0; w < LOOKBACK_WINDOW; ++w) {
+                    if (done || used != w) break;
+                    const uint32_t st = sw[w] >> STATUS_COUNT_BITS;
+                    if (st == st_agg || st == st_inc) {
+                        excl += sw[w] & STATUS_COUNT_MASK;
+                        used = w + 1;
+                        done = (st == st_inc);
+                    }
+                }
+                if (done) break;
+                lb_next -= used;
+                if (used == 0) {
+                    if (++polls > prm.spin_limit) {
+                        record_error(hdr, ERR_LOOKBACK_TIMEOUT, ((uint32_t)prm.pass << 24) | (tile & 0xFFFFFFu));
+                        break;
+                    }
+                    __nanosleep(polls < 64 ? 32 : 256);
+                }
+            }
+            if (!faulty)
+                st_relaxed_gpu(my_status + tid, (st_inc << STATUS_COUNT_BITS) | ((excl + cnt) & STATUS_COUNT_MASK));
+        }
+        sm.binoff[tid] = dbase + excl - local;
     }
     __syncthreads();
 
-    // ---- coalesced scatter: consecutive slots of one digit go to consecutive
-    //      global positions ---------------------------------------------------
-    for (uint32_t j = tid; j < valid; j += THREADS) {
-        const K key = sm.keys[j];
-        const uint32_t d = digit_of(key, prm.shift, prm.mask);
-        const uint32_t pos = sm.binoff[d] + j;
-        kdst[pos] = last ? KeyCodec<K>::dec(key, prm.kind, flip) : key;
-        if (PAIRS) vdst[pos] = sm.vals[j];
-    }
+    if (last)
+        store_tile<true, BYTE, K, PAIRS, THREADS>(sm.keys, sm.vals, sm.binoff, valid, kdst, vdst, prm, tid);
+    else
+        store_tile<false, BYTE, K, PAIRS, THREADS>(sm.keys, sm.vals, sm.binoff, valid, kdst, vdst, prm, tid);
 }
 
 // ---------------------------------------------------------------------------
@@ -497,16 +708,25 @@ cudaError_t launch_hist(const RadixJob &job, cudaStream_t stream, bool plan, int
     return cudaGetLastError();
 }
 
-template <typename K, bool PAIRS, int THREADS, int ITEMS>
-cudaError_t launch_passes(const RadixJob &job, cudaStream_t stream, int *launches) {
+template <typename K, bool PAIRS, int THREADS, int ITEMS, bool BYTE> cudaError_t configure_pass() {
     using S = PassSmem<K, PAIRS, THREADS, ITEMS>;
-    auto kern = onesweep_pass_kernel<K, PAIRS, THREADS, ITEMS>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(S));
+        cudaError_t e = cudaFuncSetAttribute(onesweep_pass_kernel<K, PAIRS, THREADS, ITEMS, BYTE>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(S));
         if (e != cudaSuccess) return e;
         configured = true;
     }
+    return cudaSuccess;
+}
+
+template <typename K, bool PAIRS, int THREADS, int ITEMS>
+cudaError_t launch_passes(const RadixJob &job, cudaStream_t stream, int *launches) {
+    using S = PassSmem<K, PAIRS, THREADS, ITEMS>;
+    const bool byte_digits = (job.begin_bit % 8) == 0;
+    cudaError_t e = byte_digits ? configure_pass<K, PAIRS, THREADS, ITEMS, true>()
+                                : configure_pass<K, PAIRS, THREADS, ITEMS, false>();
+    if (e != cudaSuccess) return e;
     PassParams prm;
     prm.keys_in = job.keys_in;
     prm.keys_out = job.keys_out;
@@ -515,8 +735,12 @@ cudaError_t launch_passes(const RadixJob &job, cudaStream_t stream, int *launche
     prm.vals_out = job.vals_out;
     prm.vals_alt = job.vals_alt;
     prm.n = (uint32_t)job.n;
-    prm.kind = job.kind;
     prm.flip = job.descending ? ~0ull : 0ull;
+    {
+        const uint32_t f = job.descending ? 0xFFFFFFFFu : 0u;
+        prm.enc_a = job.kind == KIND_F32 ? 0x7FFFFFFFu : 0u;
+        prm.enc_b = ((job.kind == KIND_F32 || job.kind == KIND_I32) ? 0x80000000u : 0u) ^ f;
+    }
     prm.num_passes = job.num_passes;
     prm.in_place = job.in_place ? 1 : 0;
     prm.hdr = job.hdr;
@@ -524,16 +748,25 @@ cudaError_t launch_passes(const RadixJob &job, cudaStream_t stream, int *launche
     prm.spin_limit = job.spin_limit;
     prm.fault_pass = job.fault_pass;
     prm.fault_tile = job.fault_tile;
+    prm.digit_base = job.digit_base;
     for (int p = 0; p < job.num_passes; ++p) {
         prm.pass = p;
         prm.shift = job.begin_bit + 8 * p;
         const int bits = std::min(8, job.end_bit - prm.shift);
         prm.mask = (1u << bits) - 1u;
-        prm.digit_base = job.digit_base;
-        kern<<<job.num_tiles, THREADS, sizeof(S), stream>>>(prm);
+        prm.perm_sel = 0x4440u | (uint32_t)((prm.shift & 31) >> 3);
+        if (byte_digits && bits == 8)
+            onesweep_pass_kernel<K, PAIRS, THREADS, ITEMS, true><<<job.num_tiles, THREADS, sizeof(S), stream>>>(prm);
+        else {
+            if (byte_digits) {
+                e = configure_pass<K, PAIRS, THREADS, ITEMS, false>();
+                if (e != cudaSuccess) return e;
+            }
+            onesweep_pass_kernel<K, PAIRS, THREADS, ITEMS, false><<<job.num_tiles, THREADS, sizeof(S), stream>>>(prm);
+        }
         ++*launches;
         timing_mark(stream);
-        cudaError_t e = cudaGetLastError();
+        e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -541,9 +774,12 @@ cudaError_t launch_passes(const RadixJob &job, cudaStream_t stream, int *launche
 
 }  // namespace
 
-// Tile shapes: 512 threads per CTA, two CTAs per SM; 16 keys per thread for
-// 32-bit keys and 8 for 64-bit keys, so a tile is 32 KiB of keys.
-uint32_t radix_tile_keys(int key_bytes, bool /*pairs*/) { return key_bytes == 8 ? 512u * 8u : 512u * 16u; }
+// Tile shapes: 512 threads per CTA, two CTAs per SM.  32-bit keys: 24 keys
+// per thread (48 KiB tile), 16 with values; 64-bit keys: 8 per thread.
+uint32_t radix_tile_keys(int key_bytes, bool pairs) {
+    if (key_bytes == 8) return 512u * 8u;
+    return (uint32_t)GBS_U32_THREADS * (pairs ? GBS_U32_PAIR_ITEMS : GBS_U32_ITEMS);
+}
 
 cudaError_t launch_histograms(const RadixJob &job, cudaStream_t stream, int *launches) {
     if (job.key_bytes == 8) return launch_hist<uint64_t>(job, stream, false, launches);
@@ -560,8 +796,8 @@ cudaError_t launch_radix_sort(const RadixJob &job, cudaStream_t stream, int *lau
     } else {
         e = launch_hist<uint32_t>(job, stream, true, launches);
         if (e != cudaSuccess) return e;
-        e = job.pairs ? launch_passes<uint32_t, true, 512, 16>(job, stream, launches)
-                      : launch_passes<uint32_t, false, 512, 16>(job, stream, launches);
+        e = job.pairs ? launch_passes<uint32_t, true, GBS_U32_THREADS, GBS_U32_PAIR_ITEMS>(job, stream, launches)
+                      : launch_passes<uint32_t, false, GBS_U32_THREADS, GBS_U32_ITEMS>(job, stream, launches);
     }
     if (e != cudaSuccess) return e;
     if (job.in_place) {

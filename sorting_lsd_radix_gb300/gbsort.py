@@ -242,12 +242,18 @@ _timing_keepalive = None
 
 
 def gbs_debug_set_timing_events(events) -> None:
-    """events: list of torch.cuda.Event(enable_timing=True), or None to switch the hook off."""
+    """events: list of torch.cuda.Event(enable_timing=True), or None to switch the hook off.
+
+    torch creates an event's CUDA handle on its first record, so unrecorded
+    events are recorded once here first."""
     global _timing_keepalive
     if not events:
         _timing_keepalive = None
         load().gbs_debug_set_timing_events(None, 0)
         return
+    for e in events:
+        if not e.cuda_event:
+            e.record()
     arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _timing_keepalive = (arr, list(events))
     load().gbs_debug_set_timing_events(arr, len(events))

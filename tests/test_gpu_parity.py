@@ -51,7 +51,7 @@ def with_ties(dtype, n, seed, k=37):
     return base[(wl.uniform_u32(n, wl.seed_for(71, seed)) % np.uint32(k)).astype(np.int64)]
 
 
-TILE32 = 8192
+TILE32 = 12288
 SIZES = [0, 1, 2, 31, 32, 33, 1023, 4095, 4096, 4097, TILE32 - 1, TILE32, TILE32 + 1, 16383, 16384, 16385,
          3 * TILE32 + 5, (1 << 16) + 7, (1 << 20) + 3]
 
@@ -61,8 +61,27 @@ SIZES = [0, 1, 2, 31, 32, 33, 1023, 4095, 4096, 4097, TILE32 - 1, TILE32, TILE32
 @pytest.mark.parametrize("n", SIZES)
 def test_sort_keys_full_range(g, dtype, desc, n):
     keys = sample(dtype, n, n)
-    got = _host(g.gbs_sort_keys(_dev(keys), descending=desc))
-    assert np.array_equal(_u(got), _u(oracle.sort_keys(keys, descending=desc)))
+    out, temp = g.gbs_sort_keys(_dev(keys), descending=desc, return_temp=True)
+    assert np.array_equal(_u(_host(out)), _u(oracle.sort_keys(keys, descending=desc)))
+    assert g.gbs_get_status(temp) == g.GBS_OK
+
+
+def test_repeated_large_sorts_report_no_timeout(g):
+    # many tiles per pass and repeated calls on one work buffer: every device
+    # wait must end well inside its bound (a timeout would be recorded)
+    n = (1 << 24) + 12345
+    keys = wl.uniform_u32(n, wl.seed_for(2, 9))
+    d = _dev(keys)
+    out, temp = g.gbs_sort_keys(d, return_temp=True)
+    for _ in range(8):
+        g.gbs_sort_keys(d, keys_out=out, temp=temp)
+        assert g.gbs_get_status(temp) == g.GBS_OK
+    vals = torch.arange(n, dtype=torch.int32, device="cuda").view(torch.uint32) if hasattr(torch, "uint32") else None
+    assert np.array_equal(_host(out), oracle.sort_keys(keys))
+    if vals is not None:
+        for _ in range(4):
+            ko, vo, t2 = g.gbs_sort_pairs(d, vals, begin_bit=0, end_bit=32, return_temp=True)
+            assert g.gbs_get_status(t2) == g.GBS_OK
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -106,7 +125,7 @@ def test_distributions_u32(g, dist, desc):
     got = _host(g.gbs_sort_keys(_dev(keys), descending=desc))
     assert np.array_equal(got, oracle.sort_keys(keys, descending=desc))
     vals = np.arange(n, dtype=np.uint32)
-    ko, vo = g.gbs_sort_pairs(_dev(keys), _dev(vals), 0, 16, descending=desc)
+    ko, vo = g.gbs_sort_pairs(_dev(keys), _dev(vals), begin_bit=0, end_bit=16, descending=desc)
     ek, ev = oracle.sort_pairs(keys, vals, 0, 16, descending=desc)
     assert np.array_equal(_host(ko), ek) and np.array_equal(_host(vo), ev)
 
