@@ -129,6 +129,33 @@ gbs_status gbs_digit_histograms(void *d_temp, size_t *temp_bytes, gbs_key_type k
                                 int descending, uint32_t *d_hist, void *stream);
 
 /*
+ * gbs_sort_keys_noalloc — gbs_sort_keys (same key types, bit range, order
+ * and result) for callers that cannot allocate device memory: plug-ins
+ * inside an application that owns every allocation, real-time loops that
+ * cannot afford cudaMalloc's latency and implicit synchronisation, or
+ * processes whose memory pool is fixed up front.  The web pages have no
+ * counterpart to this entry point.
+ *
+ * The caller passes only its keys; the work buffer is one array of about
+ * 8.4 MiB in the library's own device memory, which every GPU that loads the
+ * library holds until the process exits.  No cudaMalloc, cudaFree or other
+ * allocating call is made.
+ *   n  at most GBS_NOALLOC_MAX_KEYS; larger n returns GBS_ERR_UNSUPPORTED
+ *      and launches nothing.
+ * The first call on each device looks up the array's device address (a
+ * cudaGetSymbolAddress with that device current); make that first call
+ * before any stream capture.  Every call, on every stream, shares the one
+ * array: calls whose work overlaps on the GPU race and corrupt each other's
+ * results, so serialise them (one stream, or events).  The array keeps the
+ * last call's contents; each call clears what it needs to start at zero.
+ * Device-side timeouts are recorded in the array's header and are not
+ * reported by gbs_get_status.
+ */
+#define GBS_NOALLOC_MAX_KEYS ((size_t)1 << 20)
+gbs_status gbs_sort_keys_noalloc(gbs_key_type key_type, const void *d_keys_in, void *d_keys_out, size_t n,
+                                 int begin_bit, int end_bit, int descending, void *stream);
+
+/*
  * gbs_get_status — synchronises `stream`, then reports GBS_ERR_TIMEOUT if the
  * last call that used this work buffer recorded a device-side timeout, else
  * GBS_OK (GBS_ERR_CUDA if the stream reports an error).  temp_bytes is the

@@ -35,7 +35,8 @@ _KIND_BYTES = {GBS_U32: 4, GBS_I32: 4, GBS_F32: 4, GBS_U64: 8}
 # every symbol the headers declare
 EXPORTS = ("gbs_sort_keys", "gbs_sort_pairs", "gbs_segmented_sort", "gbs_digit_histograms", "gbs_get_status",
            "gbs_status_string", "gbs_version", "gbs_debug_set_lookback_fault", "gbs_debug_last_launch_count",
-           "gbs_debug_radix_tile_keys", "gbs_debug_set_timing_events")
+           "gbs_debug_radix_tile_keys", "gbs_debug_set_timing_events", "gbs_sort_keys_noalloc")
+GBS_NOALLOC_MAX_KEYS = 1 << 20
 
 
 class GbsError(RuntimeError):
@@ -66,6 +67,8 @@ def load(path: str | None = None):
     lib.gbs_segmented_sort.restype = i
     lib.gbs_digit_histograms.argtypes = [vp, szp, i, vp, sz, i, i, i, vp, vp]
     lib.gbs_digit_histograms.restype = i
+    lib.gbs_sort_keys_noalloc.argtypes = [i, vp, vp, sz, i, i, i, vp]
+    lib.gbs_sort_keys_noalloc.restype = i
     lib.gbs_get_status.argtypes = [vp, sz, vp]
     lib.gbs_get_status.restype = i
     lib.gbs_status_string.argtypes = [i]
@@ -223,6 +226,27 @@ def gbs_digit_histograms(keys: torch.Tensor, begin_bit: int = 0, end_bit: int | 
     args = (kind, _ptr(keys), n, begin_bit, end_bit, int(bool(descending)), _ptr(hist), _stream(stream))
     _run(load().gbs_digit_histograms, args, temp, "gbs_digit_histograms")
     return hist[:passes]
+
+
+def gbs_sort_keys_noalloc(keys_in: torch.Tensor, keys_out: torch.Tensor, begin_bit: int = 0,
+                          end_bit: int | None = None, descending: bool = False, key_type: int | None = None,
+                          stream=None) -> torch.Tensor:
+    """gbs_sort_keys without a work buffer, for callers that cannot allocate device memory.
+
+    keys_out must be allocated by the caller (it may be keys_in); nothing is
+    allocated here either.  n <= GBS_NOALLOC_MAX_KEYS; calls share one
+    library-owned scratch array, so they must not overlap on the GPU."""
+    kind = _kind(keys_in, key_type)
+    n = keys_in.numel()
+    _check_tensor(keys_in, n, "keys_in")
+    _check_tensor(keys_out, n, "keys_out")
+    if end_bit is None:
+        end_bit = 8 * _KIND_BYTES[kind]
+    st = load().gbs_sort_keys_noalloc(kind, _ptr(keys_in), _ptr(keys_out), n, begin_bit, end_bit,
+                                      int(bool(descending)), _stream(stream))
+    if st != GBS_OK:
+        raise GbsError(st, "gbs_sort_keys_noalloc")
+    return keys_out
 
 
 def gbs_get_status(temp: torch.Tensor, stream=None) -> int:
