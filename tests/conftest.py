@@ -8,3 +8,4 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (runs the CUDA library)")
+    config.addinivalue_line("markers", "fullsize: GPU parity at the benchmark workloads' full sizes (minutes)")
