@@ -46,36 +46,34 @@ __device__ __forceinline__ uint32_t excl_scan_256(uint32_t v, uint32_t *wsum) {
 // ---------------------------------------------------------------------------
 // Peer mask: the lanes of the (fully active) warp whose 8-bit digit equals
 // this lane's.  One ballot per digit bit gives the warp's eight bit planes.
-// Lane l then builds the peer mask of the nibble value l & 15 — over planes
-// 0..3 for lanes 0..15 (low nibble) and planes 4..7 for lanes 16..31 (high
-// nibble) — and every lane fetches the masks of its own two nibbles with two
-// shuffles; their AND is the peer mask.  Must be called by all 32 lanes.
+// Lane l builds two table entries: the mask of lanes whose low five digit
+// bits equal l (planes 0..4) and the mask of lanes whose top three bits equal
+// l & 7 (planes 5..7).  Every lane then fetches the entries of its own low and
+// high part with two shuffles (the low index is the digit itself: a shuffle
+// uses its source lane modulo 32); their AND is the peer mask.  Must be called
+// by all 32 lanes.
 // ---------------------------------------------------------------------------
-struct NibbleLane {
-    uint32_t s0, s1, s2, s3;  // all ones where bit k of (lane & 15) is set
-    bool high;
-    __device__ __forceinline__ explicit NibbleLane(int lane) {
-        const uint32_t v = (uint32_t)lane & 15u;
-        s0 = 0u - (v & 1u);
-        s1 = 0u - ((v >> 1) & 1u);
-        s2 = 0u - ((v >> 2) & 1u);
-        s3 = 0u - ((v >> 3) & 1u);
-        high = lane >= 16;
+struct PeerTableLane {
+    uint32_t s[5];  // all ones where bit k of the lane index is set
+    __device__ __forceinline__ explicit PeerTableLane(int lane) {
+#pragma unroll
+        for (int k = 0; k < 5; ++k) s[k] = 0u - (((uint32_t)lane >> k) & 1u);
     }
 };
 
-__device__ __forceinline__ void warp_peer_halves(uint32_t d, const NibbleLane &nl, uint32_t &e_lo,
+__device__ __forceinline__ void warp_peer_halves(uint32_t d, const PeerTableLane &tl, uint32_t &e_lo,
                                                  uint32_t &e_hi) {
     uint32_t b[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) b[k] = __ballot_sync(FULL, (d >> k) & 1u);
-    const uint32_t p0 = nl.high ? b[4] : b[0];
-    const uint32_t p1 = nl.high ? b[5] : b[1];
-    const uint32_t p2 = nl.high ? b[6] : b[2];
-    const uint32_t p3 = nl.high ? b[7] : b[3];
-    const uint32_t e = ~(p0 ^ nl.s0) & ~(p1 ^ nl.s1) & ~(p2 ^ nl.s2) & ~(p3 ^ nl.s3);
-    e_lo = __shfl_sync(FULL, e, (int)(d & 15u));         // lanes agreeing on the low nibble
-    e_hi = __shfl_sync(FULL, e, (int)(16u + (d >> 4)));  // ... and on the high nibble
+    for (int k = 0; k < 8; ++k) b[k] = __ballot_sync(FULL, (d & (1u << k)) != 0u);
+    uint32_t lo = ~(b[0] ^ tl.s[0]);
+#pragma unroll
+    for (int k = 1; k < 5; ++k) lo &= ~(b[k] ^ tl.s[k]);
+    uint32_t hi = ~(b[5] ^ tl.s[0]);
+#pragma unroll
+    for (int k = 1; k < 3; ++k) hi &= ~(b[5 + k] ^ tl.s[k]);
+    e_lo = __shfl_sync(FULL, lo, (int)d);         // lanes agreeing on digit bits 0..4
+    e_hi = __shfl_sync(FULL, hi, (int)(d >> 5));  // ... and on bits 5..7
 }
 
 // ---------------------------------------------------------------------------
@@ -316,7 +314,7 @@ template <int ITEMS> struct PackedRanks {
 template <bool ENC, bool BYTE, bool FULLTILE, typename K, int ITEMS>
 __device__ __forceinline__ void rank_warp(const K *tile_keys, uint32_t *whist, const PassParams &prm, int warp,
                                           int lane, uint32_t valid, K (&keys)[ITEMS], PackedRanks<ITEMS> &ranks) {
-    const NibbleLane nl(lane);
+    const PeerTableLane nl(lane);
     const uint32_t lt = lanemask_lt();
 #pragma unroll
     for (int i = 0; i < ITEMS; ++i) {
