@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--n", type=int, default=N_KEYS)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="headline", choices=["headline"] + sorted(SECONDARY),
+                    help="headline: the benchmark line; others: the remaining configurations, one JSON line each")
     return ap.parse_args()
 
 
@@ -309,10 +311,130 @@ def run_gbsort(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------
+# Secondary workloads (the other configurations; informative lines, not the
+# benchmark line).  Each entry: description, builder(n) -> (call, n_keys,
+# algorithmic bytes per call, dominant-kernel algorithmic bytes per launch,
+# dominant-kernel launch indices, extra fields).
+# ---------------------------------------------------------------------------
+
+def _sec_radix_keys(gen, n, key_type, begin=0, end=None, desc=False):
+    def build(gbsort, torch):
+        keys = gen(n)
+        d = torch.from_numpy(keys).cuda()
+        o = torch.empty_like(d)
+        _, temp = gbsort.gbs_sort_keys(d, o, begin_bit=begin, end_bit=end, descending=desc, return_temp=True)
+        s = keys.itemsize
+        bits = (end if end is not None else 8 * s) - begin
+        passes = (bits + 7) // 8
+        call = lambda: gbsort.gbs_sort_keys(d, o, begin_bit=begin, end_bit=end, descending=desc, temp=temp)
+        return call, temp, n, s * n + passes * 2 * s * n, 2 * s * n, list(range(1, 1 + passes)), {}
+    return build
+
+
+def _sec_pairs_u64(n):
+    def build(gbsort, torch):
+        keys = wl.priority_u64(n, wl.seed_for(4, 0))
+        d = torch.from_numpy(keys).cuda()
+        v = torch.arange(n, dtype=torch.int32, device="cuda").view(torch.uint32)
+        ko, vo = torch.empty_like(d), torch.empty_like(v)
+        _, _, temp = gbsort.gbs_sort_pairs(d, v, ko, vo, return_temp=True)
+        call = lambda: gbsort.gbs_sort_pairs(d, v, ko, vo, temp=temp)
+        # bits 56..63 are zero: 7 active passes of 8 (the eighth returns at once)
+        return call, temp, n, 8 * n + 7 * 24 * n, 24 * n, list(range(1, 8)), {"active_passes": 7}
+    return build
+
+
+def _sec_segmented(segs, seg_len):
+    def build(gbsort, torch):
+        keys = wl.uniform_u32(segs * seg_len, wl.seed_for(2, 0))
+        d = torch.from_numpy(keys).cuda()
+        o = torch.empty_like(d)
+        call = lambda: gbsort.gbs_segmented_sort(d, segs, seg_len, keys_out=o)
+        call()
+        p = (seg_len - 1).bit_length()
+        comps = segs * (1 << p) // 2 * p * (p + 1) // 2
+        n = segs * seg_len
+        return call, None, n, 8 * n, 8 * n, [0], {"comparators_per_call": comps}
+    return build
+
+
+SECONDARY = {
+    "u32_1e8_low_entropy": ("sort_keys u32 n=1e8, AND of three uniform draws",
+                            _sec_radix_keys(lambda n: wl.low_entropy_u32(n, wl.seed_for(3, 1)), N_KEYS, "u32")),
+    "u32_1e8_sorted": ("sort_keys u32 n=1e8, already ascending",
+                       _sec_radix_keys(lambda n: wl.ascending_u32(n, wl.seed_for(3, 1)), N_KEYS, "u32")),
+    "u32_1e8_reverse": ("sort_keys u32 n=1e8, descending input",
+                        _sec_radix_keys(lambda n: wl.descending_u32(n, wl.seed_for(3, 1)), N_KEYS, "u32")),
+    "u32_1e8_all_equal": ("sort_keys u32 n=1e8, all keys equal (every pass trivial: histogram + copy)",
+                          _sec_radix_keys(lambda n: wl.all_equal_u32(n, wl.seed_for(3, 1)), N_KEYS, "u32")),
+    "u32_1e8_bits0_16": ("sort_keys u32 n=1e8 uniform, bits [0,16)",
+                         _sec_radix_keys(lambda n: wl.uniform_u32(n, SEED), N_KEYS, "u32", 0, 16)),
+    "f32_2p28": ("sort_keys f32 n=2^28, N(0,1000) with signed zeros and infinities",
+                 _sec_radix_keys(lambda n: wl.normal_mix_f32(n, wl.seed_for(5, 0)), 1 << 28, "f32")),
+    "f32_2p28_desc": ("sort_keys f32 n=2^28 descending",
+                      _sec_radix_keys(lambda n: wl.normal_mix_f32(n, wl.seed_for(5, 0)), 1 << 28, "f32",
+                                      desc=True)),
+    "i32_2p28": ("sort_keys i32 n=2^28 uniform", _sec_radix_keys(lambda n: wl.uniform_i32(n, wl.seed_for(5, 1)),
+                                                                 1 << 28, "i32")),
+    "pairs_u64_2p27": ("sort_pairs u64 keys (4-bit priority << 48 | 48-bit field) + u32 index values, n=2^27",
+                       _sec_pairs_u64(1 << 27)),
+    "seg_16384x1024": ("segmented_sort u32, 16384 segments x 1024 keys", _sec_segmented(16384, 1024)),
+    "seg_4096x16384": ("segmented_sort u32, 4096 segments x 16384 keys", _sec_segmented(4096, 16384)),
+}
+
+
+def run_secondary(args):
+    import torch
+    torch.cuda.set_device(0)
+    from sorting_lsd_radix_gb300 import build as gbuild
+    gbuild.build()
+    from sorting_lsd_radix_gb300 import gbsort
+    desc, builder = SECONDARY[args.workload]
+    call, temp, n, alg_bytes, dom_bytes, dom_idx, extra = builder(gbsort, torch)
+    torch.cuda.synchronize()
+    launches = gbsort.gbs_debug_last_launch_count()
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        call()
+    steps = max(args.steps // 10, 5)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(launches + 1)] for _ in range(steps)]
+    for evs in events:
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s_ in range(steps):
+        gbsort.gbs_debug_set_timing_events(events[s_])
+        call()
+    e1.record(stream)
+    gbsort.gbs_debug_set_timing_events(None)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    per_kernel = np.array([[ev[i].elapsed_time(ev[i + 1]) for i in range(launches)] for ev in events]).mean(axis=0)
+    dom_ms = float(per_kernel[dom_idx].mean())
+    peak, peak_kind = peaks()
+    line = {"workload": args.workload, "description": desc, "n": n, "ms_per_call": ms,
+            "keys_per_s": n / (ms / 1e3), "algorithmic_bytes": alg_bytes,
+            "achieved_gbs": alg_bytes / (ms / 1e3) / 1e9, "frac_of_peak": alg_bytes / (ms / 1e3) / 1e9 / peak,
+            "dominant_kernel_ms": dom_ms, "dominant_kernel_gbs": dom_bytes / (dom_ms / 1e3) / 1e9,
+            "dominant_kernel_frac": dom_bytes / (dom_ms / 1e3) / 1e9 / peak, "peak_gbs": peak,
+            "peak_kind": f"{peak_kind} hbm_gbs", "kernel_ms": per_kernel.tolist(), "launches": launches}
+    if "comparators_per_call" in extra:
+        line["comparators_per_s"] = extra["comparators_per_call"] / (ms / 1e3)
+    line.update({k: v for k, v in extra.items() if k != "comparators_per_call"})
+    if temp is not None:
+        line["status"] = gbsort.status_string(gbsort.gbs_get_status(temp))
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "headline":
+        run_secondary(args)
     else:
         run_gbsort(args)
 

@@ -80,16 +80,24 @@ __device__ __forceinline__ void warp_peer_halves(uint32_t d, const PeerTableLane
 // Upfront histogram of all digit passes (one read of the keys)
 // ---------------------------------------------------------------------------
 
-constexpr int HIST_THREADS = 512;
+constexpr int HIST_THREADS = 1024;  // one CTA per SM
 constexpr int HIST_UNROLL = 4;
 
+// Counters live in per-lane columns: counter (pass p, digit d) of column c is
+// word (p*256 + d) * COLS + c, and lane l uses column l % COLS.  With 32
+// columns every lane of a warp hits its own bank, so the shared-memory
+// atomics of one instruction never conflict (the columns are shared by the
+// CTA's warps, whose atomics are separate instructions).
 template <typename K> struct HistCfg;
 template <> struct HistCfg<uint32_t> {
-    static constexpr int PASSES = 4, COPIES = 8, PER_VEC = 4;
+    static constexpr int PASSES = 4, COLS = 32, PER_VEC = 4;
 };
 template <> struct HistCfg<uint64_t> {
-    static constexpr int PASSES = 8, COPIES = 4, PER_VEC = 2;
+    static constexpr int PASSES = 8, COLS = 16, PER_VEC = 2;
 };
+template <typename K> constexpr size_t hist_smem_bytes() {
+    return (size_t)HistCfg<K>::PASSES * 256 * HistCfg<K>::COLS * sizeof(uint32_t);
+}
 
 struct HistParams {
     const void *keys;
@@ -105,19 +113,18 @@ struct HistParams {
 };
 
 template <typename K>
-__global__ void __launch_bounds__(HIST_THREADS) upfront_histogram_kernel(const HistParams prm) {
+__global__ void __launch_bounds__(HIST_THREADS, 1) upfront_histogram_kernel(const HistParams prm) {
     using C = HistCfg<K>;
-    __shared__ uint32_t sh[C::COPIES * C::PASSES * 256];
+    extern __shared__ __align__(16) uint32_t sh[];
     __shared__ uint32_t wsum[8];
     __shared__ uint32_t s_last;
     const int tid = threadIdx.x;
+    const int P = prm.num_passes;
 
-    for (int i = tid; i < C::COPIES * C::PASSES * 256; i += HIST_THREADS) sh[i] = 0;
+    for (int i = tid; i < P * 256 * C::COLS; i += HIST_THREADS) sh[i] = 0;
     __syncthreads();
 
-    // privatised copy: warps take turns so that one copy serves few warps
-    uint32_t *my = sh + ((tid >> 5) % C::COPIES) * (C::PASSES * 256);
-    const int P = prm.num_passes;
+    uint32_t *my = sh + (tid & 31) % C::COLS;
     int shift[C::PASSES];
     uint32_t mask[C::PASSES];
 #pragma unroll
@@ -132,7 +139,7 @@ __global__ void __launch_bounds__(HIST_THREADS) upfront_histogram_kernel(const H
         const K t = KeyCodec<K>::enc(raw, prm.kind, flip);
 #pragma unroll
         for (int p = 0; p < C::PASSES; ++p)
-            if (p < P) atomicAdd(&my[p * 256 + digit_of(t, shift[p], mask[p])], 1u);
+            if (p < P) atomicAdd(&my[(p * 256 + digit_of(t, shift[p], mask[p])) * C::COLS], 1u);
     };
 
     const size_t n = prm.n;
@@ -170,8 +177,8 @@ __global__ void __launch_bounds__(HIST_THREADS) upfront_histogram_kernel(const H
     __syncthreads();
     for (int b = tid; b < P * 256; b += HIST_THREADS) {
         uint32_t s = 0;
-#pragma unroll
-        for (int c = 0; c < C::COPIES; ++c) s += sh[c * C::PASSES * 256 + b];
+#pragma unroll 8
+        for (int c = 0; c < C::COLS; ++c) s += sh[b * C::COLS + ((c + b) % C::COLS)];  // rotated: no conflicts
         if (s) atomicAdd(&prm.hist[b], s);
     }
     if (!prm.plan) return;
@@ -275,9 +282,23 @@ template <bool BYTE> __device__ __forceinline__ uint32_t pass_digit(uint64_t t, 
     return digit_of(t, p.shift, p.mask);
 }
 
+// dst[lo, hi) = src[lo, hi) by the CTA's threads, 16 bytes at a time when both
+// ranges are 16-byte aligned.
 template <typename K>
 __device__ __forceinline__ void copy_range(const K *src, K *dst, size_t lo, size_t hi, int tid, int nthreads) {
-    for (size_t i = lo + tid; i < hi; i += nthreads) dst[i] = src[i];
+    const K *s = src + lo;
+    K *d = dst + lo;
+    const size_t cnt = hi - lo;
+    size_t done = 0;
+    if (((reinterpret_cast<uintptr_t>(s) | reinterpret_cast<uintptr_t>(d)) & 15) == 0) {
+        constexpr size_t PER = 16 / sizeof(K);
+        const size_t nv = cnt / PER;
+        const uint4 *sv = reinterpret_cast<const uint4 *>(s);
+        uint4 *dv = reinterpret_cast<uint4 *>(d);
+        for (size_t i = tid; i < nv; i += nthreads) dv[i] = __ldcs(sv + i);
+        done = nv * PER;
+    }
+    for (size_t i = done + tid; i < cnt; i += nthreads) d[i] = s[i];
 }
 
 // Stable warp rank of a full tile's keys (see the kernel); ENC applies the
@@ -696,11 +717,18 @@ cudaError_t launch_hist(const RadixJob &job, cudaStream_t stream, bool plan, int
     prm.zero_ptr = reinterpret_cast<uint4 *>(job.status);
     prm.zero_vec = plan ? (size_t)job.num_tiles * 256 * 4 / 16 : 0;
     prm.plan = plan ? 1 : 0;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(upfront_histogram_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)hist_smem_bytes<K>());
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
     const size_t per_cta = (size_t)HIST_THREADS * HIST_UNROLL * HistCfg<K>::PER_VEC;
     size_t grid = std::max<size_t>((job.n + per_cta - 1) / per_cta, (prm.zero_vec + HIST_THREADS - 1) / HIST_THREADS);
-    grid = std::min<size_t>(grid, (size_t)device_sms() * 2);
+    grid = std::min<size_t>(grid, (size_t)device_sms());
     grid = std::max<size_t>(grid, 1);
-    upfront_histogram_kernel<K><<<(unsigned)grid, HIST_THREADS, 0, stream>>>(prm);
+    upfront_histogram_kernel<K><<<(unsigned)grid, HIST_THREADS, hist_smem_bytes<K>(), stream>>>(prm);
     ++*launches;
     timing_mark(stream);
     return cudaGetLastError();
