@@ -328,10 +328,9 @@ template <int ITEMS> struct PackedRanks {
 // input order.  Lanes holding the same digit find each other (peer mask); the
 // highest of them advances the warp's counter for that digit by the group
 // size with one shared-memory atomic and hands the old value to its peers.
-// The peer masks of two consecutive items are formed before their counter
-// updates, which stay in item order.  ENC applies the key code on load
-// (first active pass).  Output: keys (coded) and their ranks within the warp's
-// digit groups; whist ends holding the warp's digit counts.
+// ENC applies the key code on load (first active pass).  Output: keys (coded)
+// and their ranks within the warp's digit groups; whist ends holding the
+// warp's digit counts.
 template <bool ENC, bool BYTE, bool FULLTILE, typename K, int ITEMS>
 __device__ __forceinline__ void rank_warp(const K *tile_keys, uint32_t *whist, const PassParams &prm, int warp,
                                           int lane, uint32_t valid, K (&keys)[ITEMS], PackedRanks<ITEMS> &ranks) {
@@ -345,34 +344,29 @@ __device__ __forceinline__ void rank_warp(const K *tile_keys, uint32_t *whist, c
         keys[i] = key;
     }
 #pragma unroll
-    for (int i = 0; i < ITEMS; i += 2) {
-        uint32_t peers[2], d[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            if (i + u < ITEMS) {
-                d[u] = pass_digit<BYTE>(keys[i + u], prm);
-                uint32_t e_lo, e_hi;
-                warp_peer_halves(d[u], nl, e_lo, e_hi);
-                peers[u] = e_lo & e_hi;
-                if (!FULLTILE) {
-                    const uint32_t idx = (uint32_t)warp * (ITEMS * 32) + (i + u) * 32 + lane;
-                    const bool ok = idx < valid;
-                    const uint32_t vmask = __ballot_sync(FULL, ok);
-                    peers[u] &= ok ? vmask : 0u;
-                }
-            }
+    for (int i = 0; i < ITEMS; ++i) {
+        const uint32_t d = pass_digit<BYTE>(keys[i], prm);
+        uint32_t e_lo, e_hi;
+        warp_peer_halves(d, nl, e_lo, e_hi);
+        uint32_t peers = e_lo & e_hi;
+        bool ok = true;
+        if (!FULLTILE) {
+            const uint32_t idx = (uint32_t)warp * (ITEMS * 32) + i * 32 + lane;
+            ok = idx < valid;
+            const uint32_t vmask = __ballot_sync(FULL, ok);
+            peers &= ok ? vmask : 0u;
         }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            if (i + u < ITEMS) {
-                const bool ok = FULLTILE || peers[u] != 0u;
-                const int leader = ok ? 31 - __clz(peers[u]) : lane;
-                uint32_t before = 0;
-                if (ok && lane == leader) before = atomicAdd(&whist[d[u]], (uint32_t)__popc(peers[u]));
-                const uint32_t b = __shfl_sync(FULL, before, leader);
-                ranks.set(i + u, ok ? b + __popc(peers[u] & lt) : 0u);
-            }
-        }
+        const int leader = ok ? 31 - __clz(peers) : lane;
+        // the leader's atomic, predicated rather than branched around
+        uint32_t before = 0;
+        const uint32_t is_leader = (ok && lane == leader) ? 1u : 0u;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\t@p atom.shared.add.u32 %0, [%2], %3;\n\t}"
+            : "+r"(before)
+            : "r"(is_leader), "r"(smem_u32(&whist[d])), "r"((uint32_t)__popc(peers))
+            : "memory");
+        const uint32_t b = __shfl_sync(FULL, before, leader);
+        ranks.set(i, ok ? b + __popc(peers & lt) : 0u);
     }
 }
 
