@@ -408,7 +408,7 @@ __device__ __forceinline__ void wait_phase(uint64_t *bar, uint32_t parity, const
 #define GBS_U32_THREADS 512
 #endif
 #ifndef GBS_U32_ITEMS
-#define GBS_U32_ITEMS 24
+#define GBS_U32_ITEMS 32
 #endif
 #ifndef GBS_U32_PAIR_ITEMS
 #define GBS_U32_PAIR_ITEMS 16
@@ -794,8 +794,8 @@ cudaError_t launch_passes(const RadixJob &job, cudaStream_t stream, int *launche
 
 }  // namespace
 
-// Tile shapes: 512 threads per CTA, two CTAs per SM.  32-bit keys: 24 keys
-// per thread (48 KiB tile), 16 with values; 64-bit keys: 8 per thread.
+// Tile shapes: 512 threads per CTA, two CTAs per SM.  32-bit keys: 32 keys
+// per thread (64 KiB tile), 16 with values; 64-bit keys: 8 per thread.
 uint32_t radix_tile_keys(int key_bytes, bool pairs) {
     if (key_bytes == 8) return 512u * 8u;
     return (uint32_t)GBS_U32_THREADS * (pairs ? GBS_U32_PAIR_ITEMS : GBS_U32_ITEMS);
