@@ -52,12 +52,33 @@ __device__ __forceinline__ uint32_t excl_scan_256(uint32_t v, uint32_t *wsum) {
 // high part with two shuffles (the low index is the digit itself: a shuffle
 // uses its source lane modulo 32); their AND is the peer mask.  Must be called
 // by all 32 lanes.
+//
+// A plane b agrees with bit k of the lane index where b ^ c_k has its bit
+// set, c_k = 0 when that lane bit is set and all ones when it is clear.
+// GBS_PEER_IMAD=1 writes b ^ c_k as b * (c_k | 1) + c_k (c_k is 0 or -1), a
+// multiply-add on the FMA pipe instead of a logic op; it needs five more
+// registers per thread and measured slower at 32 keys per thread.
 // ---------------------------------------------------------------------------
+#ifndef GBS_PEER_IMAD
+#define GBS_PEER_IMAD 0
+#endif
+
 struct PeerTableLane {
-    uint32_t s[5];  // all ones where bit k of the lane index is set
+    uint32_t c[5];  // 0 where bit k of the lane index is set, all ones where it is clear
+    uint32_t m[5];  // c[k] | 1: +1 or -1
     __device__ __forceinline__ explicit PeerTableLane(int lane) {
 #pragma unroll
-        for (int k = 0; k < 5; ++k) s[k] = 0u - (((uint32_t)lane >> k) & 1u);
+        for (int k = 0; k < 5; ++k) {
+            c[k] = (((uint32_t)lane >> k) & 1u) - 1u;
+            m[k] = c[k] | 1u;
+        }
+    }
+    __device__ __forceinline__ uint32_t agree(uint32_t b, int k) const {
+#if GBS_PEER_IMAD
+        return b * m[k] + c[k];
+#else
+        return b ^ c[k];
+#endif
     }
 };
 
@@ -65,13 +86,10 @@ __device__ __forceinline__ void warp_peer_halves(uint32_t d, const PeerTableLane
                                                  uint32_t &e_hi) {
     uint32_t b[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) b[k] = __ballot_sync(FULL, (d & (1u << k)) != 0u);
-    uint32_t lo = ~(b[0] ^ tl.s[0]);
-#pragma unroll
-    for (int k = 1; k < 5; ++k) lo &= ~(b[k] ^ tl.s[k]);
-    uint32_t hi = ~(b[5] ^ tl.s[0]);
-#pragma unroll
-    for (int k = 1; k < 3; ++k) hi &= ~(b[5 + k] ^ tl.s[k]);
+    for (int k = 0; k < 8; ++k) b[k] = ballot_bits(d, 1u << k);
+    const uint32_t lo = tl.agree(b[0], 0) & tl.agree(b[1], 1) & tl.agree(b[2], 2) & tl.agree(b[3], 3) &
+                        tl.agree(b[4], 4);
+    const uint32_t hi = tl.agree(b[5], 0) & tl.agree(b[6], 1) & tl.agree(b[7], 2);
     e_lo = __shfl_sync(FULL, lo, (int)d);         // lanes agreeing on digit bits 0..4
     e_hi = __shfl_sync(FULL, hi, (int)(d >> 5));  // ... and on bits 5..7
 }
@@ -353,7 +371,7 @@ __device__ __forceinline__ void rank_warp(const K *tile_keys, uint32_t *whist, c
         if (!FULLTILE) {
             const uint32_t idx = (uint32_t)warp * (ITEMS * 32) + i * 32 + lane;
             ok = idx < valid;
-            const uint32_t vmask = __ballot_sync(FULL, ok);
+            const uint32_t vmask = ballot_bits(ok ? 1u : 0u, 1u);
             peers &= ok ? vmask : 0u;
         }
         const int leader = ok ? 31 - __clz(peers) : lane;
@@ -401,21 +419,41 @@ __device__ __forceinline__ void wait_phase(uint64_t *bar, uint32_t parity, const
 #ifndef LOOKBACK_WINDOW
 #define LOOKBACK_WINDOW 16
 #endif
-#ifndef GBS_PASS_MINB
-#define GBS_PASS_MINB 2
+// Launch shapes of the pass kernel (threads per CTA x keys per thread).  Every
+// shape keeps PASS_THREADS_PER_SM threads resident per SM (64 registers per
+// thread); smaller CTAs give more independent tiles per SM, whose latency-bound
+// phases (tile load, look-back, scatter) then overlap other tiles' ranking.
+#ifndef GBS_PASS_THREADS_PER_SM
+#define GBS_PASS_THREADS_PER_SM 1024
 #endif
 #ifndef GBS_U32_THREADS
-#define GBS_U32_THREADS 512
+#define GBS_U32_THREADS 256
 #endif
 #ifndef GBS_U32_ITEMS
 #define GBS_U32_ITEMS 32
 #endif
+#ifndef GBS_U32_PAIR_THREADS
+#define GBS_U32_PAIR_THREADS 256
+#endif
 #ifndef GBS_U32_PAIR_ITEMS
-#define GBS_U32_PAIR_ITEMS 16
+#define GBS_U32_PAIR_ITEMS 32
+#endif
+#ifndef GBS_U64_THREADS
+#define GBS_U64_THREADS 256
+#endif
+#ifndef GBS_U64_ITEMS
+#define GBS_U64_ITEMS 16
+#endif
+#ifndef GBS_U64_PAIR_THREADS
+#define GBS_U64_PAIR_THREADS 512
+#endif
+#ifndef GBS_U64_PAIR_ITEMS
+#define GBS_U64_PAIR_ITEMS 12
 #endif
 
 template <typename K, bool PAIRS, int THREADS, int ITEMS, bool BYTE>
-__global__ void __launch_bounds__(THREADS, GBS_PASS_MINB) onesweep_pass_kernel(const PassParams prm) {
+__global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
+    onesweep_pass_kernel(const PassParams prm) {
     static_assert(THREADS * ITEMS <= 65536, "in-tile ranks are 16-bit");
     using S = PassSmem<K, PAIRS, THREADS, ITEMS>;
     constexpr int TILE = S::TILE;
@@ -794,11 +832,11 @@ cudaError_t launch_passes(const RadixJob &job, cudaStream_t stream, int *launche
 
 }  // namespace
 
-// Tile shapes: 512 threads per CTA, two CTAs per SM.  32-bit keys: 32 keys
-// per thread (64 KiB tile), 16 with values; 64-bit keys: 8 per thread.
+// Keys per tile of each launch shape (the pass kernel's tuning macros).
 uint32_t radix_tile_keys(int key_bytes, bool pairs) {
-    if (key_bytes == 8) return 512u * 8u;
-    return (uint32_t)GBS_U32_THREADS * (pairs ? GBS_U32_PAIR_ITEMS : GBS_U32_ITEMS);
+    if (key_bytes == 8) return pairs ? (uint32_t)GBS_U64_PAIR_THREADS * GBS_U64_PAIR_ITEMS
+                                     : (uint32_t)GBS_U64_THREADS * GBS_U64_ITEMS;
+    return pairs ? (uint32_t)GBS_U32_PAIR_THREADS * GBS_U32_PAIR_ITEMS : (uint32_t)GBS_U32_THREADS * GBS_U32_ITEMS;
 }
 
 cudaError_t launch_histograms(const RadixJob &job, cudaStream_t stream, int *launches) {
@@ -811,12 +849,12 @@ cudaError_t launch_radix_sort(const RadixJob &job, cudaStream_t stream, int *lau
     if (job.key_bytes == 8) {
         e = launch_hist<uint64_t>(job, stream, true, launches);
         if (e != cudaSuccess) return e;
-        e = job.pairs ? launch_passes<uint64_t, true, 512, 8>(job, stream, launches)
-                      : launch_passes<uint64_t, false, 512, 8>(job, stream, launches);
+        e = job.pairs ? launch_passes<uint64_t, true, GBS_U64_PAIR_THREADS, GBS_U64_PAIR_ITEMS>(job, stream, launches)
+                      : launch_passes<uint64_t, false, GBS_U64_THREADS, GBS_U64_ITEMS>(job, stream, launches);
     } else {
         e = launch_hist<uint32_t>(job, stream, true, launches);
         if (e != cudaSuccess) return e;
-        e = job.pairs ? launch_passes<uint32_t, true, GBS_U32_THREADS, GBS_U32_PAIR_ITEMS>(job, stream, launches)
+        e = job.pairs ? launch_passes<uint32_t, true, GBS_U32_PAIR_THREADS, GBS_U32_PAIR_ITEMS>(job, stream, launches)
                       : launch_passes<uint32_t, false, GBS_U32_THREADS, GBS_U32_ITEMS>(job, stream, launches);
     }
     if (e != cudaSuccess) return e;

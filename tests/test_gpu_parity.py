@@ -51,7 +51,10 @@ def with_ties(dtype, n, seed, k=37):
     return base[(wl.uniform_u32(n, wl.seed_for(71, seed)) % np.uint32(k)).astype(np.int64)]
 
 
-TILE32 = 16384
+# Radix tile sizes of the launch shapes: 8192 keys (u32 keys and u32 pairs),
+# 4096 (u64).  The sizes straddle each boundary, span several tiles with a
+# ragged tail, and cross the bitonic/radix switch at 16384 keys.
+TILE32 = 8192
 SIZES = [0, 1, 2, 31, 32, 33, 1023, 4095, 4096, 4097, TILE32 - 1, TILE32, TILE32 + 1, 16383, 16384, 16385,
          3 * TILE32 + 5, (1 << 16) + 7, (1 << 20) + 3]
 
