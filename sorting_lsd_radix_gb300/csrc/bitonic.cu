@@ -62,32 +62,52 @@ __device__ __forceinline__ void relayout(K (&x)[1 << K_LOG], K *row, int t) {
     for (int r = 0; r < (1 << K_LOG); ++r) x[r] = row[padded<PAD>(layout_index<K_LOG>(t, r, TO))];
 }
 
-// Compare-exchange across register bit RB in layout G0, for merge stage M.
-template <typename K, int K_LOG, int M, int G0, int RB>
-__device__ __forceinline__ void exchange_regbit(K (&x)[1 << K_LOG], int t) {
+// Direction by complement.  Within merge stage M every compare-exchange pairs
+// two elements whose index bit M is equal, so no key leaves the set of
+// positions with bit M set during the stage.  Complementing the keys held at
+// those positions for the duration of the stage turns their descending
+// compare-exchanges into ascending ones: min/max of complemented keys is the
+// complement of max/min.  Every exchange is then a plain ascending min/max,
+// and the direction costs one XOR per key per stage instead of two selects
+// per compare-exchange.
+//
+// Bit M of the segment index of register r of thread t in the blocked layout
+// (register bits [0, K_LOG), thread bits above); 0 for M < 1, where no stage
+// has run.
+template <int K_LOG, int M> __device__ __forceinline__ uint32_t blocked_bit(int t, int r) {
+    if constexpr (M < 1)
+        return 0u;
+    else if constexpr (M < K_LOG)
+        return ((uint32_t)r >> M) & 1u;
+    else
+        return ((uint32_t)t >> (M - K_LOG)) & 1u;
+}
+
+// Between stage M - 1 and stage M (blocked layout): undo the complement of
+// stage M - 1 and apply that of stage M.
+template <typename K, int K_LOG, int M> __device__ __forceinline__ void switch_direction(K (&x)[1 << K_LOG], int t) {
+#pragma unroll
+    for (int r = 0; r < (1 << K_LOG); ++r) {
+        const uint32_t b = blocked_bit<K_LOG, M - 1>(t, r) ^ blocked_bit<K_LOG, M>(t, r);
+        x[r] ^= (K)0 - (K)b;
+    }
+}
+
+// Ascending compare-exchange across register bit RB.
+template <typename K, int K_LOG, int RB> __device__ __forceinline__ void exchange_regbit(K (&x)[1 << K_LOG]) {
 #pragma unroll
     for (int r = 0; r < (1 << K_LOG); ++r) {
         if (r & (1 << RB)) continue;
         const int r2 = r | (1 << RB);
-        bool desc;
-        if constexpr (M >= G0 && M < G0 + K_LOG)
-            desc = (r >> (M - G0)) & 1;      // segment bit is a register bit
-        else if constexpr (M < G0)
-            desc = (t >> M) & 1;             // ... a low thread bit
-        else
-            desc = (t >> (M - K_LOG)) & 1;   // ... a high thread bit
         const K a = x[r], b = x[r2];
-        const K lo = a < b ? a : b;
-        const K hi = a < b ? b : a;
-        x[r] = desc ? hi : lo;
-        x[r2] = desc ? lo : hi;
+        x[r] = a < b ? a : b;
+        x[r2] = a < b ? b : a;
     }
 }
 
-template <typename K, int K_LOG, int M, int G0, int B>
-__device__ __forceinline__ void strides_down(K (&x)[1 << K_LOG], int t) {
-    exchange_regbit<K, K_LOG, M, G0, B - G0>(x, t);
-    if constexpr (B > G0) strides_down<K, K_LOG, M, G0, B - 1>(x, t);
+template <typename K, int K_LOG, int G0, int B> __device__ __forceinline__ void strides_down(K (&x)[1 << K_LOG]) {
+    exchange_regbit<K, K_LOG, B - G0>(x);
+    if constexpr (B > G0) strides_down<K, K_LOG, G0, B - 1>(x);
 }
 
 // Register-bit offset of group q: q*K_LOG, kept inside the segment's index bits.
@@ -105,14 +125,18 @@ __device__ __forceinline__ void stage_groups(K (&x)[1 << K_LOG], K *row, int t) 
     constexpr int HI = (Q == QT) ? M - 1 : PREV - 1;
     static_assert(G0 >= 0 && G0 + K_LOG <= L_LOG && HI >= G0 && HI < G0 + K_LOG, "bad register-bit group");
     if constexpr (G0 != PREV) relayout<K, K_LOG, PAD, WARP_LOCAL, PREV, G0>(x, row, t);
-    strides_down<K, K_LOG, M, G0, HI>(x, t);
+    strides_down<K, K_LOG, G0, HI>(x);
     if constexpr (Q > 0) stage_groups<K, K_LOG, PAD, WARP_LOCAL, L_LOG, M, Q - 1, QT>(x, row, t);
 }
 
+// Stages M .. L_LOG; each starts and ends in the blocked layout.  The last
+// stage complements nothing (bit L_LOG of every segment index is 0), so no
+// key is left complemented.
 template <typename K, int K_LOG, int PAD, bool WARP_LOCAL, int L_LOG, int M>
 __device__ __forceinline__ void all_stages(K (&x)[1 << K_LOG], K *row, int t) {
     if constexpr (M <= L_LOG) {
         constexpr int QT = (M - 1) / K_LOG;
+        switch_direction<K, K_LOG, M>(x, t);
         stage_groups<K, K_LOG, PAD, WARP_LOCAL, L_LOG, M, QT, QT>(x, row, t);
         all_stages<K, K_LOG, PAD, WARP_LOCAL, L_LOG, M + 1>(x, row, t);
     }

@@ -349,6 +349,13 @@ template <int ITEMS> struct PackedRanks {
 // ENC applies the key code on load (first active pass).  Output: keys (coded)
 // and their ranks within the warp's digit groups; whist ends holding the
 // warp's digit counts.
+template <bool ENC, typename K>
+__device__ __forceinline__ K load_key(const K *tile_keys, uint32_t idx, bool ok, const PassParams &prm) {
+    K key = ok ? tile_keys[idx] : (K)0;
+    if (ENC) key = Xform<K>::enc(key, prm);
+    return key;
+}
+
 template <bool ENC, bool BYTE, bool FULLTILE, typename K, int ITEMS>
 __device__ __forceinline__ void rank_warp(const K *tile_keys, uint32_t *whist, const PassParams &prm, int warp,
                                           int lane, uint32_t valid, K (&keys)[ITEMS], PackedRanks<ITEMS> &ranks) {
@@ -357,9 +364,7 @@ __device__ __forceinline__ void rank_warp(const K *tile_keys, uint32_t *whist, c
 #pragma unroll
     for (int i = 0; i < ITEMS; ++i) {
         const uint32_t idx = (uint32_t)warp * (ITEMS * 32) + i * 32 + lane;
-        K key = (FULLTILE || idx < valid) ? tile_keys[idx] : (K)0;
-        if (ENC) key = Xform<K>::enc(key, prm);
-        keys[i] = key;
+        keys[i] = load_key<ENC>(tile_keys, idx, FULLTILE || idx < valid, prm);
     }
 #pragma unroll
     for (int i = 0; i < ITEMS; ++i) {
@@ -397,8 +402,13 @@ __device__ __forceinline__ void store_tile(const K *sk, const uint32_t *sv, cons
     for (uint32_t j = tid; j < valid; j += THREADS) {
         const K key = sk[j];
         const uint32_t pos = binoff[pass_digit<BYTE>(key, prm)] + j;
-        kdst[pos] = DEC ? Xform<K>::dec(key, prm) : key;
-        if (PAIRS) vdst[pos] = sv[j];
+        // always true unless a bounded wait gave up (an error is then recorded):
+        // counts taken from a tile that never landed must not move a store out
+        // of the output
+        if (pos < prm.n) {
+            kdst[pos] = DEC ? Xform<K>::dec(key, prm) : key;
+            if (PAIRS) vdst[pos] = sv[j];
+        }
     }
 }
 
@@ -419,6 +429,104 @@ __device__ __forceinline__ void wait_phase(uint64_t *bar, uint32_t parity, const
 #ifndef LOOKBACK_WINDOW
 #define LOOKBACK_WINDOW 16
 #endif
+
+// Status words of predecessors lb_next, lb_next - 1, ... for digit d; a
+// position before tile 0 reads as an inclusive prefix of 0.
+template <int W>
+__device__ __forceinline__ void load_window(uint32_t (&sw)[W], const uint32_t *status, int32_t lb_next, int d,
+                                            uint32_t st_inc) {
+#pragma unroll
+    for (int w = 0; w < W; ++w)
+        sw[w] = (lb_next - w >= 0) ? ld_relaxed_gpu(status + (size_t)(lb_next - w) * 256 + d)
+                                   : (st_inc << STATUS_COUNT_BITS);
+}
+
+// Adds a window's counts, nearest predecessor first, through the first
+// inclusive prefix (done); stops before a predecessor that has published
+// nothing yet.  used: predecessors consumed.
+template <int W>
+__device__ __forceinline__ void add_window(const uint32_t (&sw)[W], uint32_t st_agg, uint32_t st_inc, uint32_t &excl,
+                                           int &used, bool &done) {
+    used = 0;
+    done = false;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+        if (done || used != w) break;
+        const uint32_t st = sw[w] >> STATUS_COUNT_BITS;
+        if (st == st_agg || st == st_inc) {
+            excl += sw[w] & STATUS_COUNT_MASK;
+            used = w + 1;
+            done = (st == st_inc);
+        }
+    }
+}
+
+// Exclusive prefix of digit d over the tiles before `tile` > 0 (decoupled
+// look-back): reads LOOKBACK_WINDOW predecessors per round trip, adds the
+// aggregates from the nearest one back to the first inclusive prefix, and
+// waits (bounded) only at a predecessor that has published nothing yet.
+__device__ __forceinline__ uint32_t lookback_excl(const PassParams &prm, Header *hdr, uint32_t tile, int d,
+                                                  uint32_t st_agg, uint32_t st_inc) {
+    uint32_t excl = 0;
+    int32_t lb_next = (int32_t)tile - 1;  // nearest predecessor not yet added
+    uint32_t polls = 0;
+    bool done = false;
+    while (!done) {
+        uint32_t sw[LOOKBACK_WINDOW];
+        load_window(sw, prm.status, lb_next, d, st_inc);
+        int used;
+        add_window(sw, st_agg, st_inc, excl, used, done);
+        if (done) break;
+        lb_next -= used;
+        if (used == 0) {
+            if (++polls > prm.spin_limit) {
+                record_error(hdr, ERR_LOOKBACK_TIMEOUT, ((uint32_t)prm.pass << 24) | (tile & 0xFFFFFFu));
+                break;
+            }
+            __nanosleep(polls < 64 ? 32 : 256);
+        }
+    }
+    return excl;
+}
+
+// The tile's count of digit d (thread d < 256) from the warps' counters, which
+// become each warp's exclusive offset within the digit's keys.
+template <int WARPS> __device__ __forceinline__ uint32_t tile_digit_count(uint32_t (*whist)[256], int d) {
+    uint32_t run = 0;
+#pragma unroll 4
+    for (int w = 0; w < WARPS; ++w) {
+        const uint32_t c = whist[w][d];
+        whist[w][d] = run;
+        run += c;
+    }
+    return run;
+}
+
+// Source and destination buffers of active pass number k of A.  The last
+// active pass lands in the output (or in the scratch buffer when an in-place
+// call has an odd number of active passes, which keeps every pass out of
+// place; the copy kernel then finishes).
+template <typename K, bool PAIRS> struct PassIO {
+    const K *ksrc;
+    K *kdst;
+    const uint32_t *vsrc = nullptr;
+    uint32_t *vdst = nullptr;
+    __device__ __forceinline__ PassIO(const PassParams &prm, uint32_t A, uint32_t k) {
+        const bool odd_in_place = prm.in_place && (A & 1u);
+        K *kout = reinterpret_cast<K *>(prm.keys_out), *kalt = reinterpret_cast<K *>(prm.keys_alt);
+        K *k_last = odd_in_place ? kalt : kout, *k_other = odd_in_place ? kout : kalt;
+        const bool src_last = ((A - k) & 1u) == 0, dst_last = ((A - 1 - k) & 1u) == 0;
+        ksrc = (k == 0) ? reinterpret_cast<const K *>(prm.keys_in) : (src_last ? k_last : k_other);
+        kdst = dst_last ? k_last : k_other;
+        if (PAIRS) {
+            uint32_t *v_last = odd_in_place ? prm.vals_alt : prm.vals_out;
+            uint32_t *v_other = odd_in_place ? prm.vals_out : prm.vals_alt;
+            vsrc = (k == 0) ? prm.vals_in : (src_last ? v_last : v_other);
+            vdst = dst_last ? v_last : v_other;
+        }
+    }
+};
+
 // Launch shapes of the pass kernel (threads per CTA x keys per thread).  Every
 // shape keeps PASS_THREADS_PER_SM threads resident per SM (64 registers per
 // thread); smaller CTAs give more independent tiles per SM, whose latency-bound
@@ -450,7 +558,6 @@ __device__ __forceinline__ void wait_phase(uint64_t *bar, uint32_t parity, const
 #ifndef GBS_U64_PAIR_ITEMS
 #define GBS_U64_PAIR_ITEMS 12
 #endif
-
 template <typename K, bool PAIRS, int THREADS, int ITEMS, bool BYTE>
 __global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
     onesweep_pass_kernel(const PassParams prm) {
@@ -482,22 +589,11 @@ __global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
     const uint32_t k = hdr->ordinal[prm.pass];
     const bool first = (k == 0), last = (k + 1 == A);
 
-    // buffers: the last active pass lands in the output (or in the scratch
-    // buffer when an in-place call has an odd number of active passes, which
-    // keeps every pass out of place; the copy kernel then finishes)
-    const bool odd_in_place = prm.in_place && (A & 1u);
-    K *kout = reinterpret_cast<K *>(prm.keys_out), *kalt = reinterpret_cast<K *>(prm.keys_alt);
-    K *k_last = odd_in_place ? kalt : kout, *k_other = odd_in_place ? kout : kalt;
-    const K *ksrc = first ? reinterpret_cast<const K *>(prm.keys_in) : ((((A - k) & 1u) == 0) ? k_last : k_other);
-    K *kdst = (((A - 1 - k) & 1u) == 0) ? k_last : k_other;
-    uint32_t *v_last = odd_in_place ? prm.vals_alt : prm.vals_out;
-    uint32_t *v_other = odd_in_place ? prm.vals_out : prm.vals_alt;
-    const uint32_t *vsrc = nullptr;
-    uint32_t *vdst = nullptr;
-    if (PAIRS) {
-        vsrc = first ? prm.vals_in : ((((A - k) & 1u) == 0) ? v_last : v_other);
-        vdst = (((A - 1 - k) & 1u) == 0) ? v_last : v_other;
-    }
+    const PassIO<K, PAIRS> io(prm, A, k);
+    const K *ksrc = io.ksrc;
+    K *kdst = io.kdst;
+    const uint32_t *vsrc = io.vsrc;
+    uint32_t *vdst = io.vdst;
 
     // chained-scan states of this pass (rotated by ordinal, see common.cuh)
     const uint32_t st_agg = 1u + 2u * (k % 3u), st_inc = 2u + 2u * (k % 3u);
@@ -579,15 +675,8 @@ __global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
     uint32_t *my_status = prm.status + (size_t)tile * 256;
     const bool faulty = (prm.fault_pass == prm.pass) && (prm.fault_tile == tile);
     if (tid < 256) {
-        uint32_t run = 0;
-#pragma unroll 4
-        for (int w = 0; w < WARPS; ++w) {
-            const uint32_t c = sm.whist[w][tid];
-            sm.whist[w][tid] = run;
-            run += c;
-        }
-        cnt = run;
-        if (!faulty) st_relaxed_gpu(my_status + tid, ((tile == 0 ? st_inc : st_agg) << STATUS_COUNT_BITS) | run);
+        cnt = tile_digit_count<WARPS>(sm.whist, tid);
+        if (!faulty) st_relaxed_gpu(my_status + tid, ((tile == 0 ? st_inc : st_agg) << STATUS_COUNT_BITS) | cnt);
     }
     const uint32_t local = excl_scan_256(cnt, sm.wsum);
     if (tid < 256) {
@@ -631,36 +720,7 @@ __global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
     if (tid < 256) {
         uint32_t excl = 0;
         if (tile > 0) {
-            int32_t lb_next = (int32_t)tile - 1;  // nearest predecessor not yet added
-            uint32_t polls = 0;
-            for (;;) {
-                uint32_t sw[LOOKBACK_WINDOW];
-#pragma unroll
-                for (int w = 0; w < LOOKBACK_WINDOW; ++w)
-                    sw[w] = (lb_next - w >= 0) ? ld_relaxed_gpu(prm.status + (size_t)(lb_next - w) * 256 + tid)
-                                               : (st_inc << STATUS_COUNT_BITS);
-                int used = 0;
-                bool done = false;
-#pragma unroll
-                for (int w = 0; w < LOOKBACK_WINDOW; ++w) {
-                    if (done || used != w) break;
-                    const uint32_t st = sw[w] >> STATUS_COUNT_BITS;
-                    if (st == st_agg || st == st_inc) {
-                        excl += sw[w] & STATUS_COUNT_MASK;
-                        used = w + 1;
-                        done = (st == st_inc);
-                    }
-                }
-                if (done) break;
-                lb_next -= used;
-                if (used == 0) {
-                    if (++polls > prm.spin_limit) {
-                        record_error(hdr, ERR_LOOKBACK_TIMEOUT, ((uint32_t)prm.pass << 24) | (tile & 0xFFFFFFu));
-                        break;
-                    }
-                    __nanosleep(polls < 64 ? 32 : 256);
-                }
-            }
+            excl = lookback_excl(prm, hdr, tile, tid, st_agg, st_inc);
             if (!faulty)
                 st_relaxed_gpu(my_status + tid, (st_inc << STATUS_COUNT_BITS) | ((excl + cnt) & STATUS_COUNT_MASK));
         }
@@ -766,25 +826,26 @@ cudaError_t launch_hist(const RadixJob &job, cudaStream_t stream, bool plan, int
     return cudaGetLastError();
 }
 
-template <typename K, bool PAIRS, int THREADS, int ITEMS, bool BYTE> cudaError_t configure_pass() {
+// One pass-kernel instantiation: the one-time shared-memory attribute set-up
+// and the launch of one CTA per tile.
+template <typename K, bool PAIRS, int THREADS, int ITEMS, bool BYTE> struct PassLaunch {
     using S = PassSmem<K, PAIRS, THREADS, ITEMS>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(onesweep_pass_kernel<K, PAIRS, THREADS, ITEMS, BYTE>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(S));
-        if (e != cudaSuccess) return e;
-        configured = true;
+    static cudaError_t launch(uint32_t num_tiles, const PassParams &prm, cudaStream_t stream) {
+        static bool configured = false;
+        if (!configured) {
+            cudaError_t e = cudaFuncSetAttribute(onesweep_pass_kernel<K, PAIRS, THREADS, ITEMS, BYTE>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(S));
+            if (e != cudaSuccess) return e;
+            configured = true;
+        }
+        onesweep_pass_kernel<K, PAIRS, THREADS, ITEMS, BYTE><<<num_tiles, THREADS, sizeof(S), stream>>>(prm);
+        return cudaGetLastError();
     }
-    return cudaSuccess;
-}
+};
 
 template <typename K, bool PAIRS, int THREADS, int ITEMS>
 cudaError_t launch_passes(const RadixJob &job, cudaStream_t stream, int *launches) {
-    using S = PassSmem<K, PAIRS, THREADS, ITEMS>;
     const bool byte_digits = (job.begin_bit % 8) == 0;
-    cudaError_t e = byte_digits ? configure_pass<K, PAIRS, THREADS, ITEMS, true>()
-                                : configure_pass<K, PAIRS, THREADS, ITEMS, false>();
-    if (e != cudaSuccess) return e;
     PassParams prm;
     prm.keys_in = job.keys_in;
     prm.keys_out = job.keys_out;
@@ -813,19 +874,13 @@ cudaError_t launch_passes(const RadixJob &job, cudaStream_t stream, int *launche
         const int bits = std::min(8, job.end_bit - prm.shift);
         prm.mask = (1u << bits) - 1u;
         prm.perm_sel = 0x4440u | (uint32_t)((prm.shift & 31) >> 3);
-        if (byte_digits && bits == 8)
-            onesweep_pass_kernel<K, PAIRS, THREADS, ITEMS, true><<<job.num_tiles, THREADS, sizeof(S), stream>>>(prm);
-        else {
-            if (byte_digits) {
-                e = configure_pass<K, PAIRS, THREADS, ITEMS, false>();
-                if (e != cudaSuccess) return e;
-            }
-            onesweep_pass_kernel<K, PAIRS, THREADS, ITEMS, false><<<job.num_tiles, THREADS, sizeof(S), stream>>>(prm);
-        }
+        const cudaError_t e =
+            (byte_digits && bits == 8)
+                ? PassLaunch<K, PAIRS, THREADS, ITEMS, true>::launch(job.num_tiles, prm, stream)
+                : PassLaunch<K, PAIRS, THREADS, ITEMS, false>::launch(job.num_tiles, prm, stream);
+        if (e != cudaSuccess) return e;
         ++*launches;
         timing_mark(stream);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
