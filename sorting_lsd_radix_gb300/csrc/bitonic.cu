@@ -93,6 +93,11 @@ template <typename K, int K_LOG, int M> __device__ __forceinline__ void switch_d
     }
 }
 
+__device__ __forceinline__ uint32_t key_min(uint32_t a, uint32_t b) { return umin(a, b); }
+__device__ __forceinline__ uint32_t key_max(uint32_t a, uint32_t b) { return umax(a, b); }
+__device__ __forceinline__ uint64_t key_min(uint64_t a, uint64_t b) { return a < b ? a : b; }
+__device__ __forceinline__ uint64_t key_max(uint64_t a, uint64_t b) { return a < b ? b : a; }
+
 // Ascending compare-exchange across register bit RB.
 template <typename K, int K_LOG, int RB> __device__ __forceinline__ void exchange_regbit(K (&x)[1 << K_LOG]) {
 #pragma unroll
@@ -100,8 +105,8 @@ template <typename K, int K_LOG, int RB> __device__ __forceinline__ void exchang
         if (r & (1 << RB)) continue;
         const int r2 = r | (1 << RB);
         const K a = x[r], b = x[r2];
-        x[r] = a < b ? a : b;
-        x[r2] = a < b ? b : a;
+        x[r] = key_min(a, b);
+        x[r2] = key_max(a, b);
     }
 }
 
@@ -151,8 +156,23 @@ struct BitonicParams {
     uint64_t flip;
 };
 
+// Resident threads per SM the kernel is compiled for (registers per thread =
+// 65536 / this); 0 leaves the register count to the compiler.  More resident
+// CTAs let one segment's global load and store overlap another's network.
+#ifndef GBS_BITONIC_THREADS_PER_SM_32
+#define GBS_BITONIC_THREADS_PER_SM_32 1024
+#endif
+#ifndef GBS_BITONIC_THREADS_PER_SM_64
+#define GBS_BITONIC_THREADS_PER_SM_64 0
+#endif
+template <typename K, int T> constexpr int bitonic_min_blocks() {
+    constexpr int per_sm = sizeof(K) == 8 ? GBS_BITONIC_THREADS_PER_SM_64 : GBS_BITONIC_THREADS_PER_SM_32;
+    return per_sm / T > 1 ? per_sm / T : 1;
+}
+
 template <typename K, int L_LOG, int K_LOG>
-__global__ void __launch_bounds__(Shape<K, L_LOG, K_LOG>::T) bitonic_tile_kernel(const BitonicParams prm) {
+__global__ void __launch_bounds__(Shape<K, L_LOG, K_LOG>::T, (bitonic_min_blocks<K, Shape<K, L_LOG, K_LOG>::T>()))
+    bitonic_tile_kernel(const BitonicParams prm) {
     using Sh = Shape<K, L_LOG, K_LOG>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     K *sm = reinterpret_cast<K *>(smem_raw);
@@ -165,13 +185,32 @@ __global__ void __launch_bounds__(Shape<K, L_LOG, K_LOG>::T) bitonic_tile_kernel
     const K flip = (K)prm.flip;
     const uint32_t len = prm.seg_len;
 
-    // coalesced load of this CTA's segments, encoded, padded with all-ones
-    for (int e = tid; e < Sh::SEGS * Sh::L; e += Sh::T) {
-        const int s = e >> L_LOG, i = e & (Sh::L - 1);
-        const size_t seg = seg0 + s;
-        K v = KeyCodec<K>::ALL_ONES;
-        if (seg < prm.num_segments && (uint32_t)i < len) v = KeyCodec<K>::enc(in[seg * len + i], prm.kind, flip);
-        sm[s * Sh::LP + padded<Sh::PAD>(i)] = v;
+    // coalesced load of this CTA's segments, encoded, padded with all-ones.
+    // Whole segments of the padded length on 16-byte boundaries (the usual
+    // case) move as 16-byte vectors; a vector never straddles a segment or a
+    // shared-memory pad (both are multiples of the vector's keys).
+    constexpr int VEC = 16 / (int)sizeof(K);
+    const bool vec = Sh::L % VEC == 0 && len == (uint32_t)Sh::L && seg0 + Sh::SEGS <= prm.num_segments &&
+                     ((reinterpret_cast<uintptr_t>(in + seg0 * len) | reinterpret_cast<uintptr_t>(out + seg0 * len)) &
+                      15) == 0;
+    if (vec) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(in + seg0 * len);
+        for (int e = tid; e < Sh::SEGS * Sh::L / VEC; e += Sh::T) {
+            const uint4 w = __ldcs(src + e);
+            const K *ks = reinterpret_cast<const K *>(&w);
+            const int k0 = e * VEC, s = k0 >> L_LOG, i = k0 & (Sh::L - 1);
+            K *dst = sm + s * Sh::LP + padded<Sh::PAD>(i);
+#pragma unroll
+            for (int u = 0; u < VEC; ++u) dst[u] = KeyCodec<K>::enc(ks[u], prm.kind, flip);
+        }
+    } else {
+        for (int e = tid; e < Sh::SEGS * Sh::L; e += Sh::T) {
+            const int s = e >> L_LOG, i = e & (Sh::L - 1);
+            const size_t seg = seg0 + s;
+            K v = KeyCodec<K>::ALL_ONES;
+            if (seg < prm.num_segments && (uint32_t)i < len) v = KeyCodec<K>::enc(in[seg * len + i], prm.kind, flip);
+            sm[s * Sh::LP + padded<Sh::PAD>(i)] = v;
+        }
     }
     __syncthreads();
     K x[Sh::KP];
@@ -184,11 +223,24 @@ __global__ void __launch_bounds__(Shape<K, L_LOG, K_LOG>::T) bitonic_tile_kernel
 #pragma unroll
     for (int r = 0; r < Sh::KP; ++r) row[padded<Sh::PAD>(layout_index<K_LOG>(t, r, 0))] = x[r];
     __syncthreads();
-    for (int e = tid; e < Sh::SEGS * Sh::L; e += Sh::T) {
-        const int s = e >> L_LOG, i = e & (Sh::L - 1);
-        const size_t seg = seg0 + s;
-        if (seg < prm.num_segments && (uint32_t)i < len)
-            out[seg * len + i] = KeyCodec<K>::dec(sm[s * Sh::LP + padded<Sh::PAD>(i)], prm.kind, flip);
+    if (vec) {
+        uint4 *dstv = reinterpret_cast<uint4 *>(out + seg0 * len);
+        for (int e = tid; e < Sh::SEGS * Sh::L / VEC; e += Sh::T) {
+            const int k0 = e * VEC, s = k0 >> L_LOG, i = k0 & (Sh::L - 1);
+            const K *src = sm + s * Sh::LP + padded<Sh::PAD>(i);
+            uint4 w;
+            K *ks = reinterpret_cast<K *>(&w);
+#pragma unroll
+            for (int u = 0; u < VEC; ++u) ks[u] = KeyCodec<K>::dec(src[u], prm.kind, flip);
+            __stcs(dstv + e, w);
+        }
+    } else {
+        for (int e = tid; e < Sh::SEGS * Sh::L; e += Sh::T) {
+            const int s = e >> L_LOG, i = e & (Sh::L - 1);
+            const size_t seg = seg0 + s;
+            if (seg < prm.num_segments && (uint32_t)i < len)
+                out[seg * len + i] = KeyCodec<K>::dec(sm[s * Sh::LP + padded<Sh::PAD>(i)], prm.kind, flip);
+        }
     }
 }
 
@@ -209,9 +261,11 @@ cudaError_t launch_shape(const BitonicParams &prm, cudaStream_t stream) {
 
 template <typename K, int L_LOG>
 cudaError_t launch_len(const BitonicParams &prm, cudaStream_t stream) {
-    // 32 keys per thread for 4-byte keys; 16 for 8-byte keys, except 32 at
-    // 2^14 keys, where 16 would need 1024 threads with at most 64 registers
-    constexpr int KMAX = (sizeof(K) == 8 && L_LOG < 14) ? 4 : 5;
+    // Keys per thread, chosen by measurement on GB300.  4-byte keys: 32, but 16
+    // for 2^11 and 2^12 keys (32 there needs more than the 64 registers that
+    // keep several CTAs resident).  8-byte keys: 16, but 32 at 2^14 keys,
+    // where 16 would need 1024 threads with at most 64 registers.
+    constexpr int KMAX = sizeof(K) == 8 ? (L_LOG < 14 ? 4 : 5) : (L_LOG == 11 || L_LOG == 12) ? 4 : 5;
     constexpr int K_LOG = L_LOG < KMAX ? L_LOG : KMAX;
     return launch_shape<K, L_LOG, K_LOG>(prm, stream);
 }
