@@ -94,6 +94,26 @@ gbs_status gbs_sort_keys(void *d_temp, size_t *temp_bytes, gbs_key_type key_type
                          int begin_bit, int end_bit, int descending, void *stream);
 
 /*
+ * gbs_sort_keys_host — gbs_sort_keys (same key types, bit range, order and
+ * result) on keys in HOST memory: enqueues on `stream` a copy of the n keys
+ * to the device, the sort, and a copy of the sorted keys back to h_keys_out.
+ * The web pages sort device-resident arrays; this entry point adds the two
+ * transfers around that sort for callers whose data lives on the host.
+ *   h_keys_in   host array of n keys (not modified unless equal to h_keys_out)
+ *   h_keys_out  host array of n keys; may equal h_keys_in
+ *   d_temp      device work buffer (same protocol as gbs_sort_keys: query the
+ *               size with d_temp == NULL); it holds the sort's own work buffer
+ *               followed by the keys' device copy (about n * key size more)
+ * Page-locked host buffers (cudaHostAlloc, cudaHostRegister) make both copies
+ * asynchronous; with pageable buffers the call blocks during the copies.
+ * The call returns once everything is enqueued: synchronise `stream` (or call
+ * gbs_get_status, which does) before reading h_keys_out.  The transfers run
+ * at the host link's rate, which bounds the call's throughput.
+ */
+gbs_status gbs_sort_keys_host(void *d_temp, size_t *temp_bytes, gbs_key_type key_type, const void *h_keys_in,
+                              void *h_keys_out, size_t n, int begin_bit, int end_bit, int descending, void *stream);
+
+/*
  * gbs_sort_pairs — like gbs_sort_keys, moving one uint32_t value with each
  * key.  Stable: pairs with equal codes keep their input order.
  *   d_vals_in / d_vals_out  device arrays of n uint32_t; may be equal

@@ -168,6 +168,34 @@ gbs_status gbs_sort_keys(void *d_temp, size_t *temp_bytes, gbs_key_type key_type
                         end_bit, descending, stream);
 }
 
+gbs_status gbs_sort_keys_host(void *d_temp, size_t *temp_bytes, gbs_key_type key_type, const void *h_keys_in,
+                              void *h_keys_out, size_t n, int begin_bit, int end_bit, int descending, void *stream) {
+    const int kb = key_bytes_of(key_type);
+    if (kb == 0 || temp_bytes == nullptr) return GBS_ERR_INVALID_ARG;
+    if (begin_bit < 0 || end_bit < begin_bit || end_bit > 8 * kb) return GBS_ERR_INVALID_ARG;
+    if (n > GBS_MAX_RADIX_KEYS) return GBS_ERR_UNSUPPORTED;
+    // work buffer: the in-place device sort's own work buffer first (so that
+    // gbs_get_status finds its header at d_temp), then the keys' device copy
+    size_t sort_bytes = 0;
+    gbs_status st = radix_common(nullptr, &sort_bytes, key_type, nullptr, nullptr, nullptr, nullptr, false, n,
+                                 begin_bit, end_bit, descending, stream);
+    if (st != GBS_OK) return st;
+    const size_t keys_off = round_up(sort_bytes);
+    bool query = false;
+    st = check_temp(d_temp, temp_bytes, keys_off + round_up((size_t)kb * n), &query);
+    if (st != GBS_OK || query) return st;
+    if (n > 0 && (h_keys_in == nullptr || h_keys_out == nullptr)) return GBS_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    void *d_keys = reinterpret_cast<unsigned char *>(d_temp) + keys_off;
+    if (n > 0 && cudaMemcpyAsync(d_keys, h_keys_in, n * kb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return GBS_ERR_CUDA;
+    size_t inner = keys_off;  // also clears the status header when n == 0
+    st = radix_common(d_temp, &inner, key_type, d_keys, d_keys, nullptr, nullptr, false, n, begin_bit, end_bit,
+                      descending, stream);
+    if (st != GBS_OK || n == 0) return st;
+    return from_cuda(cudaMemcpyAsync(h_keys_out, d_keys, n * kb, cudaMemcpyDeviceToHost, s));
+}
+
 gbs_status gbs_sort_pairs(void *d_temp, size_t *temp_bytes, gbs_key_type key_type, const void *d_keys_in,
                           void *d_keys_out, const uint32_t *d_vals_in, uint32_t *d_vals_out, size_t n,
                           int begin_bit, int end_bit, int descending, void *stream) {

@@ -326,9 +326,9 @@ __device__ __forceinline__ void copy_range(const K *src, K *dst, size_t lo, size
 // In-tile ranks are kept as 16-bit halves, two per register.
 template <int ITEMS> struct PackedRanks {
     uint32_t r[(ITEMS + 1) / 2];
-    __device__ __forceinline__ void set(int i, uint32_t v) {
+    __device__ __forceinline__ void set(int i, uint32_t v) {  // v < 2^16
         if (i & 1)
-            r[i >> 1] |= v << 16;
+            r[i >> 1] = __byte_perm(r[i >> 1], v, 0x5410);
         else
             r[i >> 1] = v;
     }
@@ -379,16 +379,19 @@ __device__ __forceinline__ void rank_warp(const K *tile_keys, uint32_t *whist, c
             const uint32_t vmask = ballot_bits(ok ? 1u : 0u, 1u);
             peers &= ok ? vmask : 0u;
         }
-        const int leader = ok ? 31 - __clz(peers) : lane;
+        // leader: the highest lane of the group (bfind: index of the top set
+        // bit; all ones for the empty mask of a lane past the tile's end, which
+        // then matches no lane)
+        uint32_t leader;
+        asm("bfind.u32 %0, %1;" : "=r"(leader) : "r"(peers));
         // the leader's atomic, predicated rather than branched around
         uint32_t before = 0;
-        const uint32_t is_leader = (ok && lane == leader) ? 1u : 0u;
         asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\t@p atom.shared.add.u32 %0, [%2], %3;\n\t}"
+            "{\n\t.reg .pred p;\n\tsetp.eq.u32 p, %1, %2;\n\t@p atom.shared.add.u32 %0, [%3], %4;\n\t}"
             : "+r"(before)
-            : "r"(is_leader), "r"(smem_u32(&whist[d])), "r"((uint32_t)__popc(peers))
+            : "r"((uint32_t)lane), "r"(leader), "r"(smem_u32(&whist[d])), "r"((uint32_t)__popc(peers))
             : "memory");
-        const uint32_t b = __shfl_sync(FULL, before, leader);
+        const uint32_t b = __shfl_sync(FULL, before, (int)leader);
         ranks.set(i, ok ? b + __popc(peers & lt) : 0u);
     }
 }

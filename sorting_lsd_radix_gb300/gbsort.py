@@ -35,7 +35,8 @@ _KIND_BYTES = {GBS_U32: 4, GBS_I32: 4, GBS_F32: 4, GBS_U64: 8}
 # every symbol the headers declare
 EXPORTS = ("gbs_sort_keys", "gbs_sort_pairs", "gbs_segmented_sort", "gbs_digit_histograms", "gbs_get_status",
            "gbs_status_string", "gbs_version", "gbs_debug_set_lookback_fault", "gbs_debug_last_launch_count",
-           "gbs_debug_radix_tile_keys", "gbs_debug_set_timing_events", "gbs_sort_keys_noalloc")
+           "gbs_debug_radix_tile_keys", "gbs_debug_set_timing_events", "gbs_sort_keys_noalloc",
+           "gbs_sort_keys_host")
 GBS_NOALLOC_MAX_KEYS = 1 << 20
 
 
@@ -61,6 +62,8 @@ def load(path: str | None = None):
     szp = ctypes.POINTER(ctypes.c_size_t)
     lib.gbs_sort_keys.argtypes = [vp, szp, i, vp, vp, sz, i, i, i, vp]
     lib.gbs_sort_keys.restype = i
+    lib.gbs_sort_keys_host.argtypes = [vp, szp, i, vp, vp, sz, i, i, i, vp]
+    lib.gbs_sort_keys_host.restype = i
     lib.gbs_sort_pairs.argtypes = [vp, szp, i, vp, vp, vp, vp, sz, i, i, i, vp]
     lib.gbs_sort_pairs.restype = i
     lib.gbs_segmented_sort.argtypes = [vp, szp, i, vp, vp, sz, sz, i, vp]
@@ -169,6 +172,27 @@ def gbs_sort_keys(keys_in: torch.Tensor, keys_out: torch.Tensor | None = None, b
         end_bit = 8 * _KIND_BYTES[kind]
     args = (kind, _ptr(keys_in), _ptr(keys_out), n, begin_bit, end_bit, int(bool(descending)), _stream(stream))
     temp = _run(load().gbs_sort_keys, args, temp, "gbs_sort_keys")
+    return (keys_out, temp) if return_temp else keys_out
+
+
+def gbs_sort_keys_host(keys_in: torch.Tensor, keys_out: torch.Tensor | None = None, begin_bit: int = 0,
+                       end_bit: int | None = None, descending: bool = False, temp: torch.Tensor | None = None,
+                       key_type: int | None = None, stream=None, return_temp: bool = False):
+    """gbs_sort_keys on a CPU tensor: copy to the device, sort, copy back into keys_out (a CPU tensor;
+    may be keys_in; None allocates one, page-locked when keys_in is).  Asynchronous on the stream:
+    synchronise it before reading keys_out.  temp is the device work buffer (torch uint8)."""
+    kind = _kind(keys_in, key_type)
+    n = keys_in.numel()
+    if keys_in.is_cuda or not keys_in.is_contiguous():
+        raise ValueError("keys_in must be a contiguous CPU tensor")
+    if keys_out is None:
+        keys_out = torch.empty_like(keys_in, pin_memory=keys_in.is_pinned())
+    if keys_out.is_cuda or not keys_out.is_contiguous() or keys_out.numel() != n:
+        raise ValueError(f"keys_out must be a contiguous CPU tensor of {n} elements")
+    if end_bit is None:
+        end_bit = 8 * _KIND_BYTES[kind]
+    args = (kind, _ptr(keys_in), _ptr(keys_out), n, begin_bit, end_bit, int(bool(descending)), _stream(stream))
+    temp = _run(load().gbs_sort_keys_host, args, temp, "gbs_sort_keys_host")
     return (keys_out, temp) if return_temp else keys_out
 
 

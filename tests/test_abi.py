@@ -64,6 +64,31 @@ def test_temp_query_sizes(lib):
     assert st3 == gbsort.GBS_OK and need3 == 256
 
 
+def test_host_entry_temp_holds_sort_buffer_and_device_keys(lib):
+    n = 10**6
+    _, sort_need = _query(lib, "gbs_sort_keys", gbsort.GBS_U32, None, None, n, 0, 32, 0, None)
+    st, need = _query(lib, "gbs_sort_keys_host", gbsort.GBS_U32, None, None, n, 0, 32, 0, None)
+    assert st == gbsort.GBS_OK
+    assert sort_need + 4 * n <= need < sort_need + 4 * n + 2 * 256
+    st, need64 = _query(lib, "gbs_sort_keys_host", gbsort.GBS_U64, None, None, n, 8, 40, 1, None)
+    assert st == gbsort.GBS_OK and need64 >= 2 * 8 * n
+
+
+def test_host_entry_rejects_bad_arguments(lib):
+    assert _query(lib, "gbs_sort_keys_host", 9, None, None, 10, 0, 8, 0, None)[0] == gbsort.GBS_ERR_INVALID_ARG
+    assert _query(lib, "gbs_sort_keys_host", gbsort.GBS_I32, None, None, 10, 4, 40, 0, None)[0] == \
+        gbsort.GBS_ERR_INVALID_ARG
+    assert _query(lib, "gbs_sort_keys_host", gbsort.GBS_U32, None, None, gbsort.GBS_MAX_RADIX_KEYS + 1, 0, 32,
+                  0, None)[0] == gbsort.GBS_ERR_UNSUPPORTED
+    fake = ctypes.c_void_p(1 << 40)  # never dereferenced: the checks fail first
+    have = ctypes.c_size_t(100)
+    assert lib.gbs_sort_keys_host(fake, ctypes.byref(have), gbsort.GBS_U32, fake, fake, 1000, 0, 32, 0, None) == \
+        gbsort.GBS_ERR_TEMP_TOO_SMALL
+    big = ctypes.c_size_t(1 << 30)
+    assert lib.gbs_sort_keys_host(fake, ctypes.byref(big), gbsort.GBS_U32, None, fake, 1000, 0, 32, 0, None) == \
+        gbsort.GBS_ERR_INVALID_ARG
+
+
 @pytest.mark.parametrize("begin,end", [(-1, 8), (9, 8), (0, 33)])
 def test_bad_bit_range(lib, begin, end):
     st, _ = _query(lib, "gbs_sort_keys", gbsort.GBS_U32, None, None, 10, begin, end, 0, None)

@@ -148,6 +148,32 @@ def test_in_place(g, dtype, n, bits):
     assert np.array_equal(_host(tk2), oracle.sort_keys(keys, bits[0], bits[1], descending=True))
 
 
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("n", [0, 1, 1000, 16385, 3 * TILE32 + 7])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_sort_keys_host_buffers(g, dtype, n, pinned):
+    keys = sample(dtype, n, n + 11)
+    h_in = torch.from_numpy(np.ascontiguousarray(keys))
+    if pinned:
+        h_in = h_in.pin_memory()
+    out, temp = g.gbs_sort_keys_host(h_in, descending=(n % 2 == 1), return_temp=True)
+    assert g.gbs_get_status(temp) == g.GBS_OK  # synchronises the stream
+    assert not out.is_cuda
+    assert np.array_equal(_u(out.numpy()), _u(oracle.sort_keys(keys, descending=(n % 2 == 1))))
+    assert np.array_equal(_u(h_in.numpy()), _u(keys))  # input untouched
+
+
+@pytest.mark.parametrize("bits", [(0, 32), (4, 20), (8, 8)])
+def test_sort_keys_host_in_place_bit_ranges(g, bits):
+    n = 2 * TILE32 + 13
+    keys = with_ties(np.uint32, n, 91)
+    h = torch.from_numpy(keys.copy()).pin_memory()
+    out, temp = g.gbs_sort_keys_host(h, h, begin_bit=bits[0], end_bit=bits[1], return_temp=True)
+    assert g.gbs_get_status(temp) == g.GBS_OK
+    assert out.data_ptr() == h.data_ptr()
+    assert np.array_equal(h.numpy(), oracle.sort_keys(keys, bits[0], bits[1]))
+
+
 def test_all_passes_trivial_and_skipped_passes(g):
     n = 3 * TILE32 + 9
     eq = wl.all_equal_u32(n, 1)
