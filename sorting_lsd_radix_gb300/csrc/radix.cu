@@ -262,6 +262,7 @@ struct PassParams {
     uint32_t mask;
     uint32_t perm_sel;  // byte-permute selector of the digit byte (byte-aligned passes)
     int in_place;
+    int identity;  // the key code is the identity (no transform on load or store)
     Header *hdr;
     const uint32_t *digit_base;
     uint32_t *status;
@@ -590,7 +591,9 @@ __global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
         return;
     }
     const uint32_t k = hdr->ordinal[prm.pass];
-    const bool first = (k == 0), last = (k + 1 == A);
+    // the key code is applied on the first active pass's load and undone on
+    // the last one's store, unless it is the identity (unsigned ascending)
+    const bool first = (k == 0) && !prm.identity, last = (k + 1 == A) && !prm.identity;
 
     const PassIO<K, PAIRS> io(prm, A, k);
     const K *ksrc = io.ksrc;
@@ -862,6 +865,7 @@ cudaError_t launch_passes(const RadixJob &job, cudaStream_t stream, int *launche
         const uint32_t f = job.descending ? 0xFFFFFFFFu : 0u;
         prm.enc_a = job.kind == KIND_F32 ? 0x7FFFFFFFu : 0u;
         prm.enc_b = ((job.kind == KIND_F32 || job.kind == KIND_I32) ? 0x80000000u : 0u) ^ f;
+        prm.identity = (prm.enc_a == 0u && prm.enc_b == 0u && prm.flip == 0ull) ? 1 : 0;
     }
     prm.num_passes = job.num_passes;
     prm.in_place = job.in_place ? 1 : 0;
