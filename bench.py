@@ -142,6 +142,22 @@ def dist_setup(args):
     return world, rank, local
 
 
+def max_over_ranks(value, dist, device):
+    """The largest of every rank's value (one all-reduce); the value itself on one rank.  device: where
+    the process group's backend keeps tensors ("cuda" for NCCL, "cpu" for gloo)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, n_per_rank, ms_per_step):
+    """Whole-job keys/s: every rank sorts its own n keys per step; the step time is the slowest rank's."""
+    return world * n_per_rank / (ms_per_step / 1e3)
+
+
 def cpu_baseline(n_total, seconds=10.0):
     """The oracle as it stands, single-threaded, on a bounded slice of the workload."""
     import oracle
@@ -230,11 +246,7 @@ def run_gbsort(args):
     gbsort.gbs_debug_set_timing_events(None)
     barrier()
     clocks = sampler.stop()
-    ms = start.elapsed_time(stop)
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(stop), dist, "cuda")
     ms_per_step = ms / args.steps
     status = gbsort.gbs_get_status(temp)
     per_kernel = np.array([[ev[i].elapsed_time(ev[i + 1]) for i in range(launches)] for ev in events])
@@ -259,15 +271,11 @@ def run_gbsort(args):
             gbsort.gbs_sort_keys_host(h_in, h_out, temp=htemp)
         e1.record(stream)
         barrier()
-        ems = e0.elapsed_time(e1) / k
+        ems = max_over_ranks(e0.elapsed_time(e1) / k, dist, "cuda")
         ok = ok and gbsort.gbs_get_status(htemp) == gbsort.GBS_OK
         hv = h_out.numpy()
         ok = ok and bool((hv[1:] >= hv[:-1]).all())
-        if dist is not None:
-            t = torch.tensor([ems], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * n / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": 4 * n,
+        e2e = {"value": job_throughput(world, n, ems), "unit": UNIT, "h2d_bytes_per_step": 4 * n,
                "d2h_bytes_per_step": 4 * n, "ms_per_step": ems}
 
     if rank != 0:
@@ -285,7 +293,7 @@ def run_gbsort(args):
     alg_total = 36.0 * n  # histogram read (4n) + 4 passes x 8n
     cpu = None if args.no_cpu_baseline else cpu_baseline(n)
     line = {
-        "metric": METRIC, "value": world * n / (ms_per_step / 1e3), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": job_throughput(world, n, ms_per_step), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "n": n, "key_type": "u32", "begin_bit": 0, "end_bit": 32,

@@ -1,0 +1,86 @@
+"""The multi-rank host logic of bench.py on CPU: two gloo ranks (one process
+each, rendezvous on 127.0.0.1) reduce their step times to the slowest rank's,
+the whole-job throughput counts every rank's keys, and the reference arm runs
+on rank 0 only.  No GPU is involved."""
+import importlib.util
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+WORKER = r"""
+import importlib.util, json, os, sys
+import torch.distributed as dist
+spec = importlib.util.spec_from_file_location("b", os.path.join(sys.argv[1], "bench.py"))
+b = importlib.util.module_from_spec(spec); spec.loader.exec_module(b)
+world, rank, local = b.dist_setup(None)
+dist.init_process_group("gloo", rank=rank, world_size=world)
+ms = b.max_over_ranks(1.0 + 3.0 * rank, dist, "cpu")     # rank 0: 1 ms, rank 1: 4 ms
+print(json.dumps({"rank": rank, "world": world, "local": local, "max_ms": ms,
+                  "value": b.job_throughput(world, 1000, ms)}), flush=True)
+dist.barrier()
+dist.destroy_process_group()
+"""
+
+
+def test_two_gloo_ranks_take_the_slowest_rank_and_count_all_keys():
+    pytest.importorskip("torch")
+    port = _free_port()
+    procs = []
+    for rank in range(2):
+        env = dict(os.environ, MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE="2",
+                   LOCAL_RANK=str(rank))
+        procs.append(subprocess.Popen([sys.executable, "-c", WORKER, ROOT], env=env, stdout=subprocess.PIPE,
+                                      stderr=subprocess.PIPE, text=True))
+    outs = []
+    for p in procs:
+        out, err = p.communicate(timeout=120)
+        assert p.returncode == 0, err
+        outs.append(json.loads(out.strip().splitlines()[-1]))
+    for rank, o in enumerate(outs):
+        assert o["rank"] == rank and o["world"] == 2 and o["local"] == rank
+        assert o["max_ms"] == 4.0
+        assert o["value"] == pytest.approx(2 * 1000 / 4e-3)
+
+
+def test_single_process_needs_no_group():
+    b = _bench()
+    assert b.max_over_ranks(2.5, None, "cpu") == 2.5
+    assert b.job_throughput(1, 10**8, 1.25) == pytest.approx(8e10)
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--steps", "1", "--warmup", "0"], env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
+
+
+def test_reference_arm_line_on_rank_zero():
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "keys/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
