@@ -122,6 +122,7 @@ struct HistParams {
     uint32_t n;
     int kind, begin_bit, end_bit, num_passes;
     uint64_t flip;
+    uint32_t enc_a, enc_b;  // branch-free 32-bit key code: x ^ ((x >>s 31) & enc_a) ^ enc_b
     uint32_t *hist;
     uint32_t *digit_base;
     Header *hdr;
@@ -130,7 +131,16 @@ struct HistParams {
     int plan;         // compute the pass plan in the last CTA
 };
 
-template <typename K>
+// The code of a key for the full-width histogram (no per-key switch on the
+// key kind).
+__device__ __forceinline__ uint32_t hist_code(uint32_t x, const HistParams &p) {
+    return x ^ (((uint32_t)((int32_t)x >> 31) & p.enc_a) ^ p.enc_b);
+}
+__device__ __forceinline__ uint64_t hist_code(uint64_t x, const HistParams &p) { return x ^ p.flip; }
+
+// FULL: the bit range is the whole key, so every pass's digit is one byte of
+// the code (one byte permute) and the number of passes is fixed.
+template <typename K, bool FULL>
 __global__ void __launch_bounds__(HIST_THREADS, 1) upfront_histogram_kernel(const HistParams prm) {
     using C = HistCfg<K>;
     extern __shared__ __align__(16) uint32_t sh[];
@@ -154,10 +164,19 @@ __global__ void __launch_bounds__(HIST_THREADS, 1) upfront_histogram_kernel(cons
     }
     const K flip = (K)prm.flip;
     auto count = [&](K raw) {
-        const K t = KeyCodec<K>::enc(raw, prm.kind, flip);
+        if constexpr (FULL) {
+            const K t = hist_code(raw, prm);
 #pragma unroll
-        for (int p = 0; p < C::PASSES; ++p)
-            if (p < P) atomicAdd(&my[(p * 256 + digit_of(t, shift[p], mask[p])) * C::COLS], 1u);
+            for (int p = 0; p < C::PASSES; ++p) {
+                const uint32_t w = (sizeof(K) == 8 && p >= 4) ? (uint32_t)((uint64_t)t >> 32) : (uint32_t)t;
+                atomicAdd(&my[(p * 256 + __byte_perm(w, 0u, 0x4440u | (uint32_t)(p & 3))) * C::COLS], 1u);
+            }
+        } else {
+            const K t = KeyCodec<K>::enc(raw, prm.kind, flip);
+#pragma unroll
+            for (int p = 0; p < C::PASSES; ++p)
+                if (p < P) atomicAdd(&my[(p * 256 + digit_of(t, shift[p], mask[p])) * C::COLS], 1u);
+        }
     };
 
     const size_t n = prm.n;
@@ -809,16 +828,25 @@ cudaError_t launch_hist(const RadixJob &job, cudaStream_t stream, bool plan, int
     prm.end_bit = job.end_bit;
     prm.num_passes = job.num_passes;
     prm.flip = job.descending ? ~0ull : 0ull;
+    {
+        const uint32_t f = job.descending ? 0xFFFFFFFFu : 0u;
+        prm.enc_a = job.kind == KIND_F32 ? 0x7FFFFFFFu : 0u;
+        prm.enc_b = ((job.kind == KIND_F32 || job.kind == KIND_I32) ? 0x80000000u : 0u) ^ f;
+    }
     prm.hist = job.hist;
     prm.digit_base = job.digit_base;
     prm.hdr = job.hdr;
     prm.zero_ptr = reinterpret_cast<uint4 *>(job.status);
     prm.zero_vec = plan ? (size_t)job.num_tiles * 256 * 4 / 16 : 0;
     prm.plan = plan ? 1 : 0;
+    const bool full = job.begin_bit == 0 && job.end_bit == 8 * (int)sizeof(K);
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(upfront_histogram_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)hist_smem_bytes<K>());
+        cudaError_t e = cudaFuncSetAttribute(upfront_histogram_kernel<K, true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hist_smem_bytes<K>());
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(upfront_histogram_kernel<K, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)hist_smem_bytes<K>());
         if (e != cudaSuccess) return e;
         configured = true;
     }
@@ -826,7 +854,10 @@ cudaError_t launch_hist(const RadixJob &job, cudaStream_t stream, bool plan, int
     size_t grid = std::max<size_t>((job.n + per_cta - 1) / per_cta, (prm.zero_vec + HIST_THREADS - 1) / HIST_THREADS);
     grid = std::min<size_t>(grid, (size_t)device_sms());
     grid = std::max<size_t>(grid, 1);
-    upfront_histogram_kernel<K><<<(unsigned)grid, HIST_THREADS, hist_smem_bytes<K>(), stream>>>(prm);
+    if (full)
+        upfront_histogram_kernel<K, true><<<(unsigned)grid, HIST_THREADS, hist_smem_bytes<K>(), stream>>>(prm);
+    else
+        upfront_histogram_kernel<K, false><<<(unsigned)grid, HIST_THREADS, hist_smem_bytes<K>(), stream>>>(prm);
     ++*launches;
     timing_mark(stream);
     return cudaGetLastError();
