@@ -468,18 +468,20 @@ __device__ __forceinline__ void load_window(uint32_t (&sw)[W], const uint32_t *s
 // inclusive prefix (done); stops before a predecessor that has published
 // nothing yet.  used: predecessors consumed.
 template <int W>
-__device__ __forceinline__ void add_window(const uint32_t (&sw)[W], uint32_t st_agg, uint32_t st_inc, uint32_t &excl,
-                                           int &used, bool &done) {
+__device__ __forceinline__ void add_window(const uint32_t (&sw)[W], uint32_t st_agg, uint32_t &excl, int &used,
+                                           bool &done) {
+    // this pass's states are st_agg (aggregate) and st_agg + 1 (inclusive prefix)
     used = 0;
     done = false;
 #pragma unroll
     for (int w = 0; w < W; ++w) {
-        if (done || used != w) break;
-        const uint32_t st = sw[w] >> STATUS_COUNT_BITS;
-        if (st == st_agg || st == st_inc) {
-            excl += sw[w] & STATUS_COUNT_MASK;
-            used = w + 1;
-            done = (st == st_inc);
+        const uint32_t rel = (sw[w] >> STATUS_COUNT_BITS) - st_agg;  // 0: aggregate, 1: inclusive prefix
+        if (rel > 1u) break;
+        excl += sw[w] & STATUS_COUNT_MASK;
+        used = w + 1;
+        if (rel == 1u) {
+            done = true;
+            break;
         }
     }
 }
@@ -498,7 +500,7 @@ __device__ __forceinline__ uint32_t lookback_excl(const PassParams &prm, Header 
         uint32_t sw[LOOKBACK_WINDOW];
         load_window(sw, prm.status, lb_next, d, st_inc);
         int used;
-        add_window(sw, st_agg, st_inc, excl, used, done);
+        add_window(sw, st_agg, excl, used, done);
         if (done) break;
         lb_next -= used;
         if (used == 0) {
