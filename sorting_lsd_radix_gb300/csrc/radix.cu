@@ -575,7 +575,7 @@ template <typename K, bool PAIRS> struct PassIO {
 #define GBS_U64_THREADS 256
 #endif
 #ifndef GBS_U64_ITEMS
-#define GBS_U64_ITEMS 16
+#define GBS_U64_ITEMS 20
 #endif
 #ifndef GBS_U64_PAIR_THREADS
 #define GBS_U64_PAIR_THREADS 512
