@@ -5,7 +5,7 @@ CPU-baseline leg are the only callers.  Nothing here imports, loads or shares
 code with the CUDA library; ``oracle.c`` restates the pages' algorithms on its
 own (serial LSD counting sort, recursive bitonic network, key encodings).
 
-Key kinds follow numpy dtypes: uint32, int32, float32 and uint64.
+Key kinds follow numpy dtypes: uint32, int32, float32, uint64, int64 and float64.
 """
 from __future__ import annotations
 
@@ -19,12 +19,14 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 
-KIND_U32, KIND_I32, KIND_F32, KIND_U64 = 0, 1, 2, 3
+KIND_U32, KIND_I32, KIND_F32, KIND_U64, KIND_I64, KIND_F64 = 0, 1, 2, 3, 4, 5
 _KINDS = {
     np.dtype(np.uint32): KIND_U32,
     np.dtype(np.int32): KIND_I32,
     np.dtype(np.float32): KIND_F32,
     np.dtype(np.uint64): KIND_U64,
+    np.dtype(np.int64): KIND_I64,
+    np.dtype(np.float64): KIND_F64,
 }
 
 _lib = None

@@ -22,7 +22,9 @@ int orc_key_bits(int kind) {
     case ORC_U32:
     case ORC_I32:
     case ORC_F32: return 32;
-    case ORC_U64: return 64;
+    case ORC_U64:
+    case ORC_I64:
+    case ORC_F64: return 64;
     default: return 0;
     }
 }
@@ -39,6 +41,8 @@ static uint64_t width_mask(int kind) {
  *   their order, so the [bjdmk] form is the one used.)
  * [kwkr] §3.3 and [bjdmk] §5.3: an IEEE-754 float with the sign bit set has all
  *   its bits inverted, otherwise only the sign bit is flipped.
+ * [bjdmk] §5.3: a double takes the same treatment over 64 bits; a signed
+ *   64-bit integer flips its sign bit as the 32-bit one does (§5.2).
  * Descending order is the ascending order of the complemented code.
  */
 uint64_t orc_key_transform(int kind, uint64_t raw, int descending) {
@@ -62,6 +66,15 @@ uint64_t orc_key_transform(int kind, uint64_t raw, int descending) {
     case ORC_U64:
         t = raw;
         break;
+    case ORC_I64:
+        t = raw ^ ((uint64_t)1 << 63);
+        break;
+    case ORC_F64:
+        if (raw >> 63)
+            t = ~raw;
+        else
+            t = raw ^ ((uint64_t)1 << 63);
+        break;
     default:
         return 0;
     }
@@ -84,6 +97,10 @@ uint64_t orc_key_inverse(int kind, uint64_t t, int descending) {
         return b;
     }
     case ORC_U64: return t;
+    case ORC_I64: return t ^ ((uint64_t)1 << 63);
+    case ORC_F64:
+        /* A code with the top bit set came from a non-negative double. */
+        return (t >> 63) ? t ^ ((uint64_t)1 << 63) : ~t;
     default: return 0;
     }
 }

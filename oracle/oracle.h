@@ -22,7 +22,8 @@
  *      [begin_bit, end_bit) bit range and per-byte pass order, §5.2 signed
  *      integer sign flip, §5.3 float map, §5.4 composite keys.
  *
- * Key kinds: 0 = u32, 1 = i32, 2 = f32 (raw IEEE-754 bits), 3 = u64.
+ * Key kinds: 0 = u32, 1 = i32, 2 = f32 (raw IEEE-754 bits), 3 = u64,
+ * 4 = i64, 5 = f64 (raw IEEE-754 bits).
  * Arrays are host memory owned by the caller.  Functions return 0 on success
  * and a negative number on a bad argument.
  */
@@ -36,7 +37,7 @@
 extern "C" {
 #endif
 
-enum { ORC_U32 = 0, ORC_I32 = 1, ORC_F32 = 2, ORC_U64 = 3 };
+enum { ORC_U32 = 0, ORC_I32 = 1, ORC_F32 = 2, ORC_U64 = 3, ORC_I64 = 4, ORC_F64 = 5 };
 
 /* Width in bits of a key kind (32 or 64); 0 for an unknown kind. */
 int orc_key_bits(int kind);

@@ -136,7 +136,21 @@ def normal_mix_f32(n: int, seed: int, sigma: float = 1e3) -> np.ndarray:
 
     The normal draws use the Box-Muller transform in double precision, then
     round to f32; a third draw per element picks the special positions."""
-    out = np.empty(n, dtype=np.float32)
+    return _normal_mix(n, seed, sigma, np.float32)
+
+
+def normal_mix_f64(n: int, seed: int, sigma: float = 1e3) -> np.ndarray:
+    """f64 counterpart of normal_mix_f32 (same draws, not rounded to f32)."""
+    return _normal_mix(n, seed, sigma, np.float64)
+
+
+def uniform_i64(n: int, seed: int) -> np.ndarray:
+    """Raw uniform 64-bit draws reinterpreted as signed integers (full signed range)."""
+    return uniform_u64(n, seed).view(np.int64)
+
+
+def _normal_mix(n: int, seed: int, sigma: float, dtype) -> np.ndarray:
+    out = np.empty(n, dtype=dtype)
     if n == 0:
         return out
     starts = list(range(0, n, _CHUNK))
@@ -147,11 +161,11 @@ def normal_mix_f32(n: int, seed: int, sigma: float = 1e3) -> np.ndarray:
         u2 = _unit_open(_draws_chunk(seed, s, c, 3, 1))
         sel = _hi32(_draws_chunk(seed, s, c, 3, 2)).astype(np.float64) * (1.0 / 4294967296.0)
         x = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2) * sigma
-        v = x.astype(np.float32)
-        v[sel < 0.025] = np.float32(0.0)
-        v[(sel >= 0.025) & (sel < 0.05)] = np.float32(-0.0)
-        v[(sel >= 0.05) & (sel < 0.055)] = np.float32(np.inf)
-        v[(sel >= 0.055) & (sel < 0.06)] = np.float32(-np.inf)
+        v = x.astype(dtype)
+        v[sel < 0.025] = dtype(0.0)
+        v[(sel >= 0.025) & (sel < 0.05)] = dtype(-0.0)
+        v[(sel >= 0.05) & (sel < 0.055)] = dtype(np.inf)
+        v[(sel >= 0.055) & (sel < 0.06)] = dtype(-np.inf)
         out[s:s + c] = v
 
     if len(starts) == 1:

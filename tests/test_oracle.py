@@ -11,7 +11,7 @@ import oracle
 from sorting_lsd_radix_gb300 import workloads as wl
 from tests import golden_io
 
-KINDS = [np.uint32, np.int32, np.float32, np.uint64]
+KINDS = [np.uint32, np.int32, np.float32, np.uint64, np.int64, np.float64]
 
 
 # --------------------------------------------------------------------------
@@ -168,12 +168,42 @@ def test_f32_code_order_is_value_order_exhaustive_sample():
     assert (np.diff(dcodes.astype(np.int64)) < 0).all()
 
 
-@pytest.mark.parametrize("dtype", [np.int32, np.float32, np.uint32, np.uint64])
+def test_f64_code_order_is_value_order_sample():
+    # Non-NaN doubles in increasing value order (a strided walk over the bit patterns from -inf to
+    # +inf, plus the neighbours of every power-of-two boundary near 1.0) get strictly increasing codes.
+    step = 0x00005A5A5A5A5A5B  # about 93 thousand doubles of each sign
+    neg = np.arange(0xFFF0000000000000, 0x8000000000000000, -step, dtype=np.uint64)
+    neg = np.append(neg[neg >= np.uint64(0x8000000000000000)], np.uint64(0x8000000000000000))
+    pos = np.append(np.arange(0, 0x7FF0000000000000, step, dtype=np.uint64), np.uint64(0x7FF0000000000000))
+    walk = np.concatenate([neg, pos])
+    f = walk.view(np.float64)
+    assert not np.isnan(f).any()
+    assert (np.diff(f) >= 0).all()
+    codes = oracle.transform_array(f)
+    assert (codes[1:] > codes[:-1]).all()
+    assert codes[0] == 0x000FFFFFFFFFFFFF and codes[-1] == 0xFFF0000000000000  # -inf, +inf extremes
+    z = oracle.transform_array(np.array([-0.0, 0.0], np.float64))
+    assert z[0] + np.uint64(1) == z[1]
+    # IEEE-754 patterns of -1.0 and 1.0: raw unsigned order is reversed, code order is not
+    neg1, pos1 = np.array([-1.0, 1.0], np.float64).view(np.uint64)
+    assert (int(neg1), int(pos1)) == (0xBFF0000000000000, 0x3FF0000000000000)
+    assert oracle.transform(oracle.KIND_F64, int(neg1)) < oracle.transform(oracle.KIND_F64, int(pos1))
+    dcodes = oracle.transform_array(f, descending=True)
+    assert (dcodes[1:] < dcodes[:-1]).all()
+
+
+def test_i64_code_is_offset_binary():
+    ext = np.array([-2**63, -1, 0, 1, 2**63 - 1], dtype=np.int64)
+    codes = oracle.transform_array(ext)
+    assert codes.tolist() == [0, 2**63 - 1, 2**63, 2**63 + 1, 2**64 - 1]
+
+
+@pytest.mark.parametrize("dtype", [np.int32, np.float32, np.uint32, np.uint64, np.int64, np.float64])
 def test_code_order_matches_native_comparison(dtype):
     a = _sample(dtype, 20000, 11)
     b = _sample(dtype, 20000, 12)
     ca, cb = oracle.transform_array(a), oracle.transform_array(b)
-    if dtype == np.float32:
+    if dtype in (np.float32, np.float64):
         same_zero = (a == 0) & (b == 0)
         lt = (a < b) | (same_zero & np.signbit(a) & ~np.signbit(b))
     else:
@@ -188,7 +218,11 @@ def test_code_roundtrip(dtype, desc):
     u = _uint_view(dtype)
     structured = np.array([0, 1, 0x7FFFFFFF, 0x80000000, 0x80000001, 0xFFFFFFFF, 0x7F800000, 0xFF800000],
                           dtype=np.uint64)
-    extra = structured.astype(u).view(dtype) if dtype != np.uint64 else structured
+    if np.dtype(dtype).itemsize == 8:
+        structured = np.concatenate([structured, np.array(
+            [0x7FFFFFFFFFFFFFFF, 0x8000000000000000, 0x8000000000000001, 0xFFFFFFFFFFFFFFFF,
+             0x7FF0000000000000, 0xFFF0000000000000, 0x3FF0000000000000, 0xBFF0000000000000], dtype=np.uint64)])
+    extra = structured.astype(u).view(dtype)
     a = np.concatenate([a, extra])
     back = oracle.inverse_array(oracle.transform_array(a, desc), dtype, desc)
     assert np.array_equal(back.view(u), a.view(u))
@@ -210,6 +244,10 @@ def _sample(dtype, n, seed):
         return wl.uniform_i32(n, seed)
     if dtype == np.float32:
         return wl.normal_mix_f32(n, seed)
+    if dtype == np.int64:
+        return wl.uniform_i64(n, seed)
+    if dtype == np.float64:
+        return wl.normal_mix_f64(n, seed)
     return wl.uniform_u64(n, seed)
 
 
@@ -222,7 +260,7 @@ def _few_distinct(dtype, n, seed, k=5):
 def _library_order(keys, descending, begin_bit=0, end_bit=None):
     """Stable order from numpy's stable sort on the native key (no oracle code)."""
     dtype = keys.dtype
-    if dtype == np.float32:
+    if dtype in (np.float32, np.float64):
         # value first; among the two zeros, -0.0 before +0.0
         pos_zero = (keys == 0) & ~np.signbit(keys)
         if descending:
@@ -237,8 +275,8 @@ def _library_order(keys, descending, begin_bit=0, end_bit=None):
     else:
         k = keys
     if descending:
-        if k.dtype == np.int32:
-            k = -(k.astype(np.int64))
+        if k.dtype in (np.int32, np.int64):
+            k = ~k  # -k - 1: order reversed, no overflow at the minimum
         else:
             k = np.iinfo(k.dtype).max - k
     return np.argsort(k, kind="stable")
