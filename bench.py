@@ -335,6 +335,10 @@ def _active_passes(keys, begin, end):
         u = u ^ np.where(u >> np.uint32(31), np.uint32(0xFFFFFFFF), np.uint32(0x80000000))
     elif keys.dtype == np.int32:
         u = u ^ np.uint32(0x80000000)
+    elif keys.dtype == np.float64:
+        u = u ^ np.where(u >> np.uint64(63), np.uint64(2**64 - 1), np.uint64(2**63))
+    elif keys.dtype == np.int64:
+        u = u ^ np.uint64(2**63)
     act = []
     for p, lo in enumerate(range(begin, end, 8)):
         mask = u.dtype.type((1 << min(8, end - lo)) - 1)
@@ -406,6 +410,10 @@ SECONDARY = {
     "f32_2p28_desc": ("sort_keys f32 n=2^28 descending",
                       _sec_radix_keys(lambda n: wl.normal_mix_f32(n, wl.seed_for(5, 0)), 1 << 28, "f32",
                                       desc=True)),
+    "f64_2p27": ("sort_keys f64 n=2^27, N(0,1000) with signed zeros and infinities",
+                 _sec_radix_keys(lambda n: wl.normal_mix_f64(n, wl.seed_for(6, 0)), 1 << 27, "f64")),
+    "i64_2p27": ("sort_keys i64 n=2^27 uniform", _sec_radix_keys(lambda n: wl.uniform_i64(n, wl.seed_for(6, 1)),
+                                                                  1 << 27, "i64")),
     "i32_2p28": ("sort_keys i32 n=2^28 uniform", _sec_radix_keys(lambda n: wl.uniform_i32(n, wl.seed_for(5, 1)),
                                                                  1 << 28, "i32")),
     "pairs_u64_2p27": ("sort_pairs u64 keys (4-bit priority << 48 | 48-bit field) + u32 index values, n=2^27",

@@ -62,7 +62,11 @@ typedef enum {
     GBS_F32 = 2, /* IEEE-754 binary32; code = b ^ (sign ? 0xFFFFFFFF : 0x80000000).
                     -0.0 sorts before +0.0; -inf and +inf are the extremes;
                     a NaN sorts by its bits (+NaN after +inf, -NaN before -inf). */
-    GBS_U64 = 3  /* uint64_t, sorted as unsigned */
+    GBS_U64 = 3, /* uint64_t, sorted as unsigned */
+    GBS_I64 = 4, /* int64_t, two's complement; code = x ^ 0x8000000000000000 */
+    GBS_F64 = 5  /* IEEE-754 binary64; code = b ^ (sign ? all ones : 0x8000000000000000),
+                    the f32 map over 64 bits ("GPU基数排序" §5.3): -0.0 before +0.0,
+                    infinities at the extremes, a NaN by its bits */
 } gbs_key_type;
 
 /* Largest number of keys a radix sort call accepts: per-digit counts are

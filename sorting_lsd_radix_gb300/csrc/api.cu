@@ -20,7 +20,9 @@ int key_bytes_of(gbs_key_type kt) {
     case GBS_U32:
     case GBS_I32:
     case GBS_F32: return 4;
-    case GBS_U64: return 8;
+    case GBS_U64:
+    case GBS_I64:
+    case GBS_F64: return 8;
     default: return 0;
     }
 }
@@ -159,6 +161,9 @@ void timing_mark(cudaStream_t s) {
 }  // namespace gbs
 
 static_assert(GBS_MAX_RADIX_KEYS == gbs::STATUS_COUNT_MASK, "key limit must match the status count field");
+static_assert((int)GBS_U32 == gbs::KIND_U32 && (int)GBS_I32 == gbs::KIND_I32 && (int)GBS_F32 == gbs::KIND_F32 &&
+                  (int)GBS_U64 == gbs::KIND_U64 && (int)GBS_I64 == gbs::KIND_I64 && (int)GBS_F64 == gbs::KIND_F64,
+              "the ABI's key types are the kernels' key kinds");
 
 extern "C" {
 

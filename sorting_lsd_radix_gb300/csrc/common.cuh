@@ -13,13 +13,33 @@ namespace gbs {
 // Key kinds and order-preserving codes
 // ---------------------------------------------------------------------------
 //
-// Unsigned keys are their own code.  Signed 32-bit keys flip the sign bit
+// Unsigned keys are their own code.  Signed keys flip the sign bit
 // ("GPU基数排序：从CUB工程实现到性能调优", §5.2).  Floats invert every bit
 // when the sign is set and only the sign bit otherwise (kwkr.cn notes on
-// bitonic vs LSD radix sort §3.3; "GPU基数排序" §5.3), so -0.0 gets the code
-// just below +0.0.  Descending sorts the complemented code ascending.
+// bitonic vs LSD radix sort §3.3; "GPU基数排序" §5.3, which extends the same
+// map to doubles), so -0.0 gets the code just below +0.0.  Descending sorts
+// the complemented code ascending.
 
-enum KeyKind : int { KIND_U32 = 0, KIND_I32 = 1, KIND_F32 = 2, KIND_U64 = 3 };
+enum KeyKind : int { KIND_U32 = 0, KIND_I32 = 1, KIND_F32 = 2, KIND_U64 = 3, KIND_I64 = 4, KIND_F64 = 5 };
+
+// The same codes without a switch on the kind: code(x) = x ^ ((x >>s (w-1)) & a) ^ b
+// for key width w, with a = all bits but the sign for floats (else 0) and
+// b = the sign bit for signed and float kinds (else 0), complemented when
+// descending.
+struct CodeConsts {
+    uint32_t a32, b32;
+    uint64_t a64, b64;
+};
+inline CodeConsts code_consts(int kind, bool descending) {
+    const bool fl = kind == KIND_F32 || kind == KIND_F64;
+    const bool sg = fl || kind == KIND_I32 || kind == KIND_I64;
+    CodeConsts c;
+    c.a32 = fl ? 0x7FFFFFFFu : 0u;
+    c.b32 = (sg ? 0x80000000u : 0u) ^ (descending ? 0xFFFFFFFFu : 0u);
+    c.a64 = fl ? 0x7FFFFFFFFFFFFFFFull : 0ull;
+    c.b64 = (sg ? 0x8000000000000000ull : 0ull) ^ (descending ? ~0ull : 0ull);
+    return c;
+}
 
 __host__ __device__ __forceinline__ uint32_t encode32(uint32_t x, int kind, uint32_t flip) {
     uint32_t t;
@@ -45,11 +65,21 @@ __host__ __device__ __forceinline__ uint32_t decode32(uint32_t t, int kind, uint
     return t;
 }
 
-__host__ __device__ __forceinline__ uint64_t encode64(uint64_t x, int /*kind*/, uint64_t flip) {
-    return x ^ flip;
-}
-__host__ __device__ __forceinline__ uint64_t decode64(uint64_t t, int /*kind*/, uint64_t flip) {
+__host__ __device__ __forceinline__ uint64_t encode64(uint64_t x, int kind, uint64_t flip) {
+    uint64_t t;
+    if (kind == KIND_F64)
+        t = x ^ ((uint64_t)((int64_t)x >> 63) | 0x8000000000000000ull);  // all ones if negative, else sign bit
+    else if (kind == KIND_I64)
+        t = x ^ 0x8000000000000000ull;
+    else
+        t = x;
     return t ^ flip;
+}
+__host__ __device__ __forceinline__ uint64_t decode64(uint64_t t, int kind, uint64_t flip) {
+    t ^= flip;
+    if (kind == KIND_F64) return t ^ ((uint64_t)(~((int64_t)t >> 63)) | 0x8000000000000000ull);
+    if (kind == KIND_I64) return t ^ 0x8000000000000000ull;
+    return t;
 }
 
 template <typename K> struct KeyCodec;

@@ -58,7 +58,9 @@ size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 extern "C" gbs_status gbs_sort_keys_noalloc(gbs_key_type key_type, const void *d_keys_in, void *d_keys_out,
                                             size_t n, int begin_bit, int end_bit, int descending, void *stream) {
-    const int kb = (key_type == GBS_U64) ? 8 : (key_type == GBS_U32 || key_type == GBS_I32 || key_type == GBS_F32) ? 4 : 0;
+    const int kb = (key_type == GBS_U64 || key_type == GBS_I64 || key_type == GBS_F64)   ? 8
+                   : (key_type == GBS_U32 || key_type == GBS_I32 || key_type == GBS_F32) ? 4
+                                                                                          : 0;
     if (kb == 0) return GBS_ERR_INVALID_ARG;
     if (begin_bit < 0 || end_bit < begin_bit || end_bit > 8 * kb) return GBS_ERR_INVALID_ARG;
     if (n > GBS_NOALLOC_MAX_KEYS) return GBS_ERR_UNSUPPORTED;

@@ -122,7 +122,8 @@ struct HistParams {
     uint32_t n;
     int kind, begin_bit, end_bit, num_passes;
     uint64_t flip;
-    uint32_t enc_a, enc_b;  // branch-free 32-bit key code: x ^ ((x >>s 31) & enc_a) ^ enc_b
+    uint32_t enc_a, enc_b;  // branch-free key code: x ^ ((x >>s (w-1)) & a) ^ b (code_consts)
+    uint64_t enc_a64, enc_b64;
     uint32_t *hist;
     uint32_t *digit_base;
     Header *hdr;
@@ -136,7 +137,9 @@ struct HistParams {
 __device__ __forceinline__ uint32_t hist_code(uint32_t x, const HistParams &p) {
     return x ^ (((uint32_t)((int32_t)x >> 31) & p.enc_a) ^ p.enc_b);
 }
-__device__ __forceinline__ uint64_t hist_code(uint64_t x, const HistParams &p) { return x ^ p.flip; }
+__device__ __forceinline__ uint64_t hist_code(uint64_t x, const HistParams &p) {
+    return x ^ (((uint64_t)((int64_t)x >> 63) & p.enc_a64) ^ p.enc_b64);
+}
 
 // FULL: the bit range is the whole key, so every pass's digit is one byte of
 // the code (one byte permute) and the number of passes is fixed.
@@ -273,10 +276,10 @@ struct PassParams {
     uint32_t *vals_out;
     uint32_t *vals_alt;
     uint32_t n;
-    // order-preserving code of a 32-bit key: x ^ ((x >>s 31) & enc_a) ^ enc_b;
-    // 64-bit keys: x ^ flip
+    // order-preserving code of a key: x ^ ((x >>s (w-1)) & a) ^ b (code_consts)
     uint32_t enc_a, enc_b;
-    uint64_t flip;
+    uint64_t enc_a64, enc_b64;
+    uint64_t flip;  // all ones when descending
     int pass, num_passes, shift;
     uint32_t mask;
     uint32_t perm_sel;  // byte-permute selector of the digit byte (byte-aligned passes)
@@ -302,8 +305,13 @@ template <> struct Xform<uint32_t> {
     }
 };
 template <> struct Xform<uint64_t> {
-    static __device__ __forceinline__ uint64_t enc(uint64_t x, const PassParams &p) { return x ^ p.flip; }
-    static __device__ __forceinline__ uint64_t dec(uint64_t t, const PassParams &p) { return t ^ p.flip; }
+    static __device__ __forceinline__ uint64_t enc(uint64_t x, const PassParams &p) {
+        return x ^ (((uint64_t)((int64_t)x >> 63) & p.enc_a64) ^ p.enc_b64);
+    }
+    static __device__ __forceinline__ uint64_t dec(uint64_t t, const PassParams &p) {
+        const uint64_t u = t ^ p.flip;  // code without the descending complement
+        return u ^ ((~(uint64_t)((int64_t)u >> 63) & p.enc_a64) ^ (p.enc_b64 ^ p.flip));
+    }
 };
 
 // Digit of a code for this pass.  BYTE: the digit is a whole byte of the
@@ -831,9 +839,11 @@ cudaError_t launch_hist(const RadixJob &job, cudaStream_t stream, bool plan, int
     prm.num_passes = job.num_passes;
     prm.flip = job.descending ? ~0ull : 0ull;
     {
-        const uint32_t f = job.descending ? 0xFFFFFFFFu : 0u;
-        prm.enc_a = job.kind == KIND_F32 ? 0x7FFFFFFFu : 0u;
-        prm.enc_b = ((job.kind == KIND_F32 || job.kind == KIND_I32) ? 0x80000000u : 0u) ^ f;
+        const CodeConsts c = code_consts(job.kind, job.descending);
+        prm.enc_a = c.a32;
+        prm.enc_b = c.b32;
+        prm.enc_a64 = c.a64;
+        prm.enc_b64 = c.b64;
     }
     prm.hist = job.hist;
     prm.digit_base = job.digit_base;
@@ -895,10 +905,12 @@ cudaError_t launch_passes(const RadixJob &job, cudaStream_t stream, int *launche
     prm.n = (uint32_t)job.n;
     prm.flip = job.descending ? ~0ull : 0ull;
     {
-        const uint32_t f = job.descending ? 0xFFFFFFFFu : 0u;
-        prm.enc_a = job.kind == KIND_F32 ? 0x7FFFFFFFu : 0u;
-        prm.enc_b = ((job.kind == KIND_F32 || job.kind == KIND_I32) ? 0x80000000u : 0u) ^ f;
-        prm.identity = (prm.enc_a == 0u && prm.enc_b == 0u && prm.flip == 0ull) ? 1 : 0;
+        const CodeConsts c = code_consts(job.kind, job.descending);
+        prm.enc_a = c.a32;
+        prm.enc_b = c.b32;
+        prm.enc_a64 = c.a64;
+        prm.enc_b64 = c.b64;
+        prm.identity = (sizeof(K) == 8 ? (c.a64 | c.b64) == 0ull : (c.a32 | c.b32) == 0u) ? 1 : 0;
     }
     prm.num_passes = job.num_passes;
     prm.in_place = job.in_place ? 1 : 0;

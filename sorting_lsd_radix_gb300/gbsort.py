@@ -20,7 +20,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgbsort.so")
 
 GBS_OK, GBS_ERR_INVALID_ARG, GBS_ERR_TEMP_TOO_SMALL, GBS_ERR_UNSUPPORTED, GBS_ERR_CUDA, GBS_ERR_TIMEOUT = range(6)
-GBS_U32, GBS_I32, GBS_F32, GBS_U64 = range(4)
+GBS_U32, GBS_I32, GBS_F32, GBS_U64, GBS_I64, GBS_F64 = range(6)
 GBS_MAX_RADIX_KEYS = (1 << 29) - 1
 GBS_MAX_SEGMENT_LEN = 16384
 
@@ -29,8 +29,10 @@ _DTYPE_KIND = {
     torch.int32: GBS_I32,
     torch.float32: GBS_F32,
     torch.uint64: GBS_U64,
+    torch.int64: GBS_I64,
+    torch.float64: GBS_F64,
 }
-_KIND_BYTES = {GBS_U32: 4, GBS_I32: 4, GBS_F32: 4, GBS_U64: 8}
+_KIND_BYTES = {GBS_U32: 4, GBS_I32: 4, GBS_F32: 4, GBS_U64: 8, GBS_I64: 8, GBS_F64: 8}
 
 # every symbol the headers declare
 EXPORTS = ("gbs_sort_keys", "gbs_sort_pairs", "gbs_segmented_sort", "gbs_digit_histograms", "gbs_get_status",

@@ -60,6 +60,10 @@ def test_temp_query_sizes(lib):
     assert need < 256 + 2 * 8 * 256 * 4 + tiles * 1024 + 4 * n + 4 * 256
     st2, need2 = _query(lib, "gbs_sort_pairs", gbsort.GBS_U64, None, None, None, None, n, 0, 64, 0, None)
     assert st2 == gbsort.GBS_OK and need2 >= 8 * n + 4 * n
+    for kt in (gbsort.GBS_I64, gbsort.GBS_F64):
+        st4, need4 = _query(lib, "gbs_sort_keys", kt, None, None, n, 0, 64, 1, None)
+        assert st4 == gbsort.GBS_OK and need4 >= 8 * n
+        assert _query(lib, "gbs_sort_keys", kt, None, None, n, 0, 65, 0, None)[0] == gbsort.GBS_ERR_INVALID_ARG
     st3, need3 = _query(lib, "gbs_segmented_sort", gbsort.GBS_U32, None, None, 16, 1024, 0, None)
     assert st3 == gbsort.GBS_OK and need3 == 256
 
@@ -97,6 +101,7 @@ def test_bad_bit_range(lib, begin, end):
 
 def test_bad_key_type_and_limits(lib):
     assert _query(lib, "gbs_sort_keys", 7, None, None, 10, 0, 8, 0, None)[0] == gbsort.GBS_ERR_INVALID_ARG
+    assert _query(lib, "gbs_sort_keys", 6, None, None, 10, 0, 8, 0, None)[0] == gbsort.GBS_ERR_INVALID_ARG
     assert _query(lib, "gbs_sort_keys", gbsort.GBS_U32, None, None, gbsort.GBS_MAX_RADIX_KEYS + 1, 0, 32, 0,
                   None)[0] == gbsort.GBS_ERR_UNSUPPORTED
     assert _query(lib, "gbs_segmented_sort", gbsort.GBS_U32, None, None, 4, 16385, 0, None)[0] == \

@@ -9,7 +9,7 @@ from sorting_lsd_radix_gb300 import workloads as wl
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-DTYPES = [np.uint32, np.int32, np.float32, np.uint64]
+DTYPES = [np.uint32, np.int32, np.float32, np.uint64, np.int64, np.float64]
 
 
 @pytest.fixture(scope="module")
@@ -43,6 +43,10 @@ def sample(dtype, n, seed):
         return wl.uniform_i32(n, s)
     if dtype == np.float32:
         return wl.normal_mix_f32(n, s)
+    if dtype == np.int64:
+        return wl.uniform_i64(n, s)
+    if dtype == np.float64:
+        return wl.normal_mix_f64(n, s)
     return wl.uniform_u64(n, s)
 
 
@@ -104,7 +108,9 @@ def test_sort_pairs_with_ties_stable(g, dtype, desc, n):
 BIT_RANGES = {np.uint32: [(0, 16), (3, 29), (8, 9), (0, 1), (31, 32), (5, 5), (16, 32), (0, 24)],
               np.int32: [(0, 16), (20, 32)],
               np.float32: [(0, 8), (23, 32)],
-              np.uint64: [(0, 52), (17, 64), (60, 64), (0, 8), (32, 64), (7, 7)]}
+              np.uint64: [(0, 52), (17, 64), (60, 64), (0, 8), (32, 64), (7, 7)],
+              np.int64: [(0, 40), (40, 64)],
+              np.float64: [(0, 8), (52, 64)]}
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -274,3 +280,22 @@ def test_float_special_values(g):
         for n in (30, 30000):
             got = _host(g.gbs_sort_keys(_dev(vals[:n]), descending=desc))
             assert np.array_equal(got.view(np.uint32), oracle.sort_keys(vals[:n], descending=desc).view(np.uint32))
+
+
+def test_double_special_values(g):
+    vals = np.array([np.inf, -0.0, 0.0, -np.inf, 1.0, -1.0, 5e-324, -5e-324, 1.7e308, -1.7e308,
+                     np.nextafter(1.0, 2.0), np.nextafter(-1.0, -2.0)] * 3000, dtype=np.float64)
+    for desc in (False, True):
+        for n in (36, 36000):
+            got = _host(g.gbs_sort_keys(_dev(vals[:n]), descending=desc))
+            assert np.array_equal(got.view(np.uint64), oracle.sort_keys(vals[:n], descending=desc).view(np.uint64))
+        seg = _host(g.gbs_segmented_sort(_dev(vals[:36 * 512]), 36, 512, descending=desc))
+        want = oracle.segmented_sort(vals[:36 * 512], 36, 512, descending=desc)
+        assert np.array_equal(seg.view(np.uint64), want.view(np.uint64))
+
+
+def test_int64_extremes(g):
+    ext = np.array([-2**63, 2**63 - 1, -1, 0, 1, -2**62, 2**62] * 5000, dtype=np.int64)
+    for desc in (False, True):
+        got = _host(g.gbs_sort_keys(_dev(ext), descending=desc))
+        assert np.array_equal(got, oracle.sort_keys(ext, descending=desc))
