@@ -141,6 +141,30 @@ gbs_status gbs_segmented_sort(void *d_temp, size_t *temp_bytes, gbs_key_type key
                               int descending, void *stream);
 
 /*
+ * gbs_segmented_sort_offsets — sort each of num_segments segments of any
+ * length independently, over the full key width: segment s is the keys
+ * [h_offsets[s], h_offsets[s+1]) of d_keys_in, sorted into the same places
+ * of d_keys_out.  Segments of up to GBS_MAX_SEGMENT_LEN keys run the bitonic
+ * network, each padded only to its own power of two (the pages advise
+ * against padding every segment to one common size: kwkr.cn notes §5.3);
+ * longer segments run the radix sort one after another.
+ *   h_offsets   HOST array of num_segments + 1 non-decreasing 64-bit offsets,
+ *               read during the call (the size query needs them too); each
+ *               segment at most GBS_MAX_RADIX_KEYS keys; every offset must lie
+ *               within both key arrays (not checked: the arrays' sizes are not
+ *               passed)
+ *   d_keys_out  may equal d_keys_in; keys outside the segments are not written
+ *   d_temp      work buffer (query its size with d_temp == NULL and the same
+ *               offsets): the offsets and a segment list by length class, plus
+ *               a radix work area for the longest segment above 2^14 keys
+ * Decreasing offsets return GBS_ERR_INVALID_ARG.  Device-side timeouts of the
+ * radix part are reported by gbs_get_status on d_temp (the first one wins).
+ */
+gbs_status gbs_segmented_sort_offsets(void *d_temp, size_t *temp_bytes, gbs_key_type key_type, const void *d_keys_in,
+                                      void *d_keys_out, size_t num_segments, const uint64_t *h_offsets,
+                                      int descending, void *stream);
+
+/*
  * gbs_digit_histograms — the upfront digit histograms of a radix sort on
  * their own: hist[p*256 + d] = number of keys whose digit p (bits
  * [begin_bit + 8p, min(begin_bit + 8p + 8, end_bit)) of the code,

@@ -1,6 +1,8 @@
 // C ABI of the gbsort library: argument checks, work-buffer layout, dispatch
 // between the radix path and the bitonic tile sorter, status reporting.
+#include <algorithm>
 #include <cstring>
+#include <vector>
 
 #include "../../include/gbsort.h"
 #include "../../include/gbsort_debug.h"
@@ -89,10 +91,12 @@ cudaError_t copy_if_needed(const void *src, void *dst, size_t bytes, cudaStream_
     return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s);
 }
 
+// keep_error: leave the header's error words as they are (a call made of
+// several sorts reports the first error of any of them).
 gbs_status radix_common(void *d_temp, size_t *temp_bytes, gbs_key_type kt, const void *keys_in, void *keys_out,
                         const uint32_t *vals_in, uint32_t *vals_out, bool pairs, size_t n, int begin_bit,
-                        int end_bit, int descending, void *stream) {
-    t_launches = 0;
+                        int end_bit, int descending, void *stream, bool keep_error = false) {
+    if (!keep_error) t_launches = 0;
     const int kb = key_bytes_of(kt);
     if (kb == 0) return GBS_ERR_INVALID_ARG;
     if (temp_bytes == nullptr) return GBS_ERR_INVALID_ARG;
@@ -107,7 +111,8 @@ gbs_status radix_common(void *d_temp, size_t *temp_bytes, gbs_key_type kt, const
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     unsigned char *tb = reinterpret_cast<unsigned char *>(d_temp);
-    cudaError_t e = cudaMemsetAsync(tb, 0, lay.digit_base, s);  // header + histograms
+    const size_t keep = keep_error ? 2 * sizeof(uint32_t) : 0;  // error, error_detail
+    cudaError_t e = cudaMemsetAsync(tb + keep, 0, lay.digit_base - keep, s);  // header + histograms
     if (e != cudaSuccess) return GBS_ERR_CUDA;
 
     const int passes = (end_bit - begin_bit + 7) / 8;
@@ -230,6 +235,97 @@ gbs_status gbs_segmented_sort(void *d_temp, size_t *temp_bytes, gbs_key_type key
     timing_start(s);
     return from_cuda(gbs::launch_segmented_bitonic((int)key_type, kb, d_keys_in, d_keys_out, num_segments,
                                                    segment_len, descending != 0, s, &t_launches));
+}
+
+gbs_status gbs_segmented_sort_offsets(void *d_temp, size_t *temp_bytes, gbs_key_type key_type, const void *d_keys_in,
+                                      void *d_keys_out, size_t num_segments, const uint64_t *h_offsets,
+                                      int descending, void *stream) {
+    t_launches = 0;
+    const int kb = key_bytes_of(key_type);
+    if (kb == 0 || temp_bytes == nullptr) return GBS_ERR_INVALID_ARG;
+    if (num_segments > 0xFFFFFFFFull) return GBS_ERR_UNSUPPORTED;  // 32-bit segment ids
+    if (num_segments > 0 && h_offsets == nullptr) return GBS_ERR_INVALID_ARG;
+    // bin the segments: class l in 1..14 holds lengths (2^(l-1), 2^l] (and 1 in class 1); longer
+    // segments take the radix path one by one, sharing one radix work area
+    constexpr int CLASSES = 15;
+    size_t count[CLASSES] = {};
+    size_t longest = 0;
+    for (size_t i = 0; i < num_segments; ++i) {
+        if (h_offsets[i + 1] < h_offsets[i]) return GBS_ERR_INVALID_ARG;
+        const uint64_t len = h_offsets[i + 1] - h_offsets[i];
+        if (len > GBS_MAX_RADIX_KEYS) return GBS_ERR_UNSUPPORTED;
+        if (len == 0) continue;
+        if (len > GBS_MAX_SEGMENT_LEN) {
+            longest = std::max<size_t>(longest, len);
+            continue;
+        }
+        int l = 1;
+        while ((uint64_t(1) << l) < len) ++l;
+        ++count[l];
+    }
+    // work buffer: [radix work area, or just the status header][offsets][segment ids by class]
+    size_t radix_bytes = sizeof(Header);
+    if (longest > 0) {
+        gbs_status st = radix_common(nullptr, &radix_bytes, key_type, nullptr, nullptr, nullptr, nullptr, false,
+                                     longest, 0, 8 * kb, descending, stream);
+        if (st != GBS_OK) return st;
+    }
+    const size_t off_offsets = round_up(radix_bytes);
+    const size_t off_ids = off_offsets + round_up(sizeof(uint64_t) * (num_segments + 1));
+    const size_t need = off_ids + round_up(sizeof(uint32_t) * std::max<size_t>(num_segments, 1));
+    bool query = false;
+    gbs_status st = check_temp(d_temp, temp_bytes, need, &query);
+    if (st != GBS_OK || query) return st;
+    if (num_segments > 0 && h_offsets[num_segments] > h_offsets[0] && (d_keys_in == nullptr || d_keys_out == nullptr))
+        return GBS_ERR_INVALID_ARG;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned char *tb = reinterpret_cast<unsigned char *>(d_temp);
+    if (cudaMemsetAsync(tb, 0, sizeof(Header), s) != cudaSuccess) return GBS_ERR_CUDA;
+    if (num_segments == 0) return GBS_OK;
+    // segment ids grouped by class (host staging, copied with the offsets)
+    std::vector<uint32_t> ids(num_segments);
+    size_t start[CLASSES + 1] = {};
+    for (int c = 1; c < CLASSES; ++c) start[c + 1] = start[c] + count[c];
+    std::vector<uint32_t> long_ids;
+    {
+        size_t fill[CLASSES];
+        std::copy(start, start + CLASSES, fill);
+        for (size_t i = 0; i < num_segments; ++i) {
+            const uint64_t len = h_offsets[i + 1] - h_offsets[i];
+            if (len == 0) continue;
+            if (len > GBS_MAX_SEGMENT_LEN) {
+                long_ids.push_back((uint32_t)i);
+                continue;
+            }
+            int l = 1;
+            while ((uint64_t(1) << l) < len) ++l;
+            ids[fill[l]++] = (uint32_t)i;
+        }
+    }
+    uint64_t *d_offsets = reinterpret_cast<uint64_t *>(tb + off_offsets);
+    uint32_t *d_ids = reinterpret_cast<uint32_t *>(tb + off_ids);
+    // pageable sources: the copies are staged before these calls return
+    if (cudaMemcpyAsync(d_offsets, h_offsets, sizeof(uint64_t) * (num_segments + 1), cudaMemcpyHostToDevice, s) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(d_ids, ids.data(), sizeof(uint32_t) * num_segments, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return GBS_ERR_CUDA;
+    timing_start(s);
+    for (int c = 1; c < CLASSES; ++c) {
+        if (count[c] == 0) continue;
+        const cudaError_t e = gbs::launch_listed_bitonic((int)key_type, kb, d_keys_in, d_keys_out, d_ids + start[c],
+                                                         count[c], d_offsets, c, descending != 0, s, &t_launches);
+        if (e != cudaSuccess) return GBS_ERR_CUDA;
+    }
+    for (const uint32_t id : long_ids) {
+        const size_t lo = h_offsets[id], len = h_offsets[id + 1] - lo;
+        size_t have = radix_bytes;
+        st = radix_common(d_temp, &have, key_type, static_cast<const unsigned char *>(d_keys_in) + lo * kb,
+                          static_cast<unsigned char *>(d_keys_out) + lo * kb, nullptr, nullptr, false, len, 0,
+                          8 * kb, descending, stream, /*keep_error=*/true);
+        if (st != GBS_OK) return st;
+    }
+    return GBS_OK;
 }
 
 gbs_status gbs_digit_histograms(void *d_temp, size_t *temp_bytes, gbs_key_type key_type, const void *d_keys,

@@ -150,10 +150,14 @@ __device__ __forceinline__ void all_stages(K (&x)[1 << K_LOG], K *row, int t) {
 struct BitonicParams {
     const void *keys_in;
     void *keys_out;
-    size_t num_segments;
-    uint32_t seg_len;
+    size_t num_segments;  // segments this launch sorts
+    uint32_t seg_len;     // uniform mode: every segment's length
     int kind;
     uint64_t flip;
+    // list mode (seg_ids != nullptr): the launch sorts segments seg_ids[0 ..
+    // num_segments), segment id holding keys [offsets[id], offsets[id + 1])
+    const uint32_t *seg_ids;
+    const uint64_t *offsets;
 };
 
 // Resident threads per SM the kernel is compiled for (registers per thread =
@@ -185,15 +189,41 @@ __global__ void __launch_bounds__(Shape<K, L_LOG, K_LOG>::T, (bitonic_min_blocks
     const K flip = (K)prm.flip;
     const uint32_t len = prm.seg_len;
 
+    // list mode: each of the CTA's segments has its own place and length
+    __shared__ size_t s_base[Sh::SEGS];
+    __shared__ uint32_t s_len[Sh::SEGS];
+    const bool listed = prm.seg_ids != nullptr;
+    if (listed) {
+        for (int j = tid; j < Sh::SEGS; j += Sh::T) {
+            size_t b = 0;
+            uint32_t l = 0;
+            if (seg0 + j < prm.num_segments) {
+                const uint32_t id = prm.seg_ids[seg0 + j];
+                b = (size_t)prm.offsets[id];
+                l = (uint32_t)(prm.offsets[id + 1] - prm.offsets[id]);
+            }
+            s_base[j] = b;
+            s_len[j] = l;
+        }
+        __syncthreads();
+    }
+
     // coalesced load of this CTA's segments, encoded, padded with all-ones.
     // Whole segments of the padded length on 16-byte boundaries (the usual
     // case) move as 16-byte vectors; a vector never straddles a segment or a
     // shared-memory pad (both are multiples of the vector's keys).
     constexpr int VEC = 16 / (int)sizeof(K);
-    const bool vec = Sh::L % VEC == 0 && len == (uint32_t)Sh::L && seg0 + Sh::SEGS <= prm.num_segments &&
+    const bool vec = !listed && Sh::L % VEC == 0 && len == (uint32_t)Sh::L && seg0 + Sh::SEGS <= prm.num_segments &&
                      ((reinterpret_cast<uintptr_t>(in + seg0 * len) | reinterpret_cast<uintptr_t>(out + seg0 * len)) &
                       15) == 0;
-    if (vec) {
+    if (listed) {
+        for (int e = tid; e < Sh::SEGS * Sh::L; e += Sh::T) {
+            const int s = e >> L_LOG, i = e & (Sh::L - 1);
+            K v = KeyCodec<K>::ALL_ONES;
+            if ((uint32_t)i < s_len[s]) v = KeyCodec<K>::enc(in[s_base[s] + i], prm.kind, flip);
+            sm[s * Sh::LP + padded<Sh::PAD>(i)] = v;
+        }
+    } else if (vec) {
         const uint4 *src = reinterpret_cast<const uint4 *>(in + seg0 * len);
         for (int e = tid; e < Sh::SEGS * Sh::L / VEC; e += Sh::T) {
             const uint4 w = __ldcs(src + e);
@@ -223,7 +253,13 @@ __global__ void __launch_bounds__(Shape<K, L_LOG, K_LOG>::T, (bitonic_min_blocks
 #pragma unroll
     for (int r = 0; r < Sh::KP; ++r) row[padded<Sh::PAD>(layout_index<K_LOG>(t, r, 0))] = x[r];
     __syncthreads();
-    if (vec) {
+    if (listed) {
+        for (int e = tid; e < Sh::SEGS * Sh::L; e += Sh::T) {
+            const int s = e >> L_LOG, i = e & (Sh::L - 1);
+            if ((uint32_t)i < s_len[s])
+                out[s_base[s] + i] = KeyCodec<K>::dec(sm[s * Sh::LP + padded<Sh::PAD>(i)], prm.kind, flip);
+        }
+    } else if (vec) {
         uint4 *dstv = reinterpret_cast<uint4 *>(out + seg0 * len);
         for (int e = tid; e < Sh::SEGS * Sh::L / VEC; e += Sh::T) {
             const int k0 = e * VEC, s = k0 >> L_LOG, i = k0 & (Sh::L - 1);
@@ -293,6 +329,25 @@ cudaError_t launch_by_log(int l, const BitonicParams &prm, cudaStream_t stream) 
 
 }  // namespace
 
+cudaError_t launch_listed_bitonic(int kind, int key_bytes, const void *keys_in, void *keys_out,
+                                  const uint32_t *seg_ids, size_t count, const uint64_t *offsets, int len_log,
+                                  bool descending, cudaStream_t stream, int *launches) {
+    BitonicParams prm;
+    prm.keys_in = keys_in;
+    prm.keys_out = keys_out;
+    prm.num_segments = count;
+    prm.seg_len = 0;
+    prm.kind = kind;
+    prm.flip = descending ? ~0ull : 0ull;
+    prm.seg_ids = seg_ids;
+    prm.offsets = offsets;
+    ++*launches;
+    const cudaError_t e = key_bytes == 8 ? launch_by_log<uint64_t>(len_log, prm, stream)
+                                         : launch_by_log<uint32_t>(len_log, prm, stream);
+    timing_mark(stream);
+    return e;
+}
+
 cudaError_t launch_segmented_bitonic(int kind, int key_bytes, const void *keys_in, void *keys_out,
                                      size_t num_segments, size_t segment_len, bool descending,
                                      cudaStream_t stream, int *launches) {
@@ -303,6 +358,8 @@ cudaError_t launch_segmented_bitonic(int kind, int key_bytes, const void *keys_i
     prm.seg_len = (uint32_t)segment_len;
     prm.kind = kind;
     prm.flip = descending ? ~0ull : 0ull;
+    prm.seg_ids = nullptr;
+    prm.offsets = nullptr;
     int l = 0;
     while ((size_t(1) << l) < segment_len) ++l;
     ++*launches;

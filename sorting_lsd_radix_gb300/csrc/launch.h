@@ -51,5 +51,10 @@ cudaError_t launch_histograms(const RadixJob &job, cudaStream_t stream, int *lau
 cudaError_t launch_segmented_bitonic(int kind, int key_bytes, const void *keys_in, void *keys_out,
                                      size_t num_segments, size_t segment_len, bool descending,
                                      cudaStream_t stream, int *launches);
+// The segments seg_ids[0 .. count) (segment id = keys [offsets[id],
+// offsets[id + 1]), at most 2^len_log keys each), one bitonic network each.
+cudaError_t launch_listed_bitonic(int kind, int key_bytes, const void *keys_in, void *keys_out,
+                                  const uint32_t *seg_ids, size_t count, const uint64_t *offsets, int len_log,
+                                  bool descending, cudaStream_t stream, int *launches);
 
 }  // namespace gbs

@@ -14,6 +14,7 @@ from __future__ import annotations
 import ctypes
 import os
 
+import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -38,7 +39,7 @@ _KIND_BYTES = {GBS_U32: 4, GBS_I32: 4, GBS_F32: 4, GBS_U64: 8, GBS_I64: 8, GBS_F
 EXPORTS = ("gbs_sort_keys", "gbs_sort_pairs", "gbs_segmented_sort", "gbs_digit_histograms", "gbs_get_status",
            "gbs_status_string", "gbs_version", "gbs_debug_set_lookback_fault", "gbs_debug_last_launch_count",
            "gbs_debug_radix_tile_keys", "gbs_debug_set_timing_events", "gbs_sort_keys_noalloc",
-           "gbs_sort_keys_host")
+           "gbs_sort_keys_host", "gbs_segmented_sort_offsets")
 GBS_NOALLOC_MAX_KEYS = 1 << 20
 
 
@@ -68,6 +69,8 @@ def load(path: str | None = None):
     lib.gbs_sort_keys_host.restype = i
     lib.gbs_sort_pairs.argtypes = [vp, szp, i, vp, vp, vp, vp, sz, i, i, i, vp]
     lib.gbs_sort_pairs.restype = i
+    lib.gbs_segmented_sort_offsets.argtypes = [vp, szp, i, vp, vp, sz, vp, i, vp]
+    lib.gbs_segmented_sort_offsets.restype = i
     lib.gbs_segmented_sort.argtypes = [vp, szp, i, vp, vp, sz, sz, i, vp]
     lib.gbs_segmented_sort.restype = i
     lib.gbs_digit_histograms.argtypes = [vp, szp, i, vp, sz, i, i, i, vp, vp]
@@ -236,6 +239,33 @@ def gbs_segmented_sort(keys_in: torch.Tensor, num_segments: int, segment_len: in
     args = (kind, _ptr(keys_in), _ptr(keys_out), num_segments, segment_len, int(bool(descending)), _stream(stream))
     _run(load().gbs_segmented_sort, args, temp, "gbs_segmented_sort")
     return keys_out
+
+
+def gbs_segmented_sort_offsets(keys_in: torch.Tensor, offsets, keys_out: torch.Tensor | None = None,
+                               descending: bool = False, temp: torch.Tensor | None = None,
+                               key_type: int | None = None, stream=None, return_temp: bool = False):
+    """Sorts each segment [offsets[s], offsets[s+1]) of keys_in independently (any lengths).
+
+    offsets: host sequence of num_segments + 1 non-decreasing integers (list, numpy or CPU tensor).
+    keys_out may be keys_in; None allocates a copy of keys_in, so keys outside the segments keep
+    their values."""
+    kind = _kind(keys_in, key_type)
+    n = keys_in.numel()
+    _check_tensor(keys_in, n, "keys_in")
+    if isinstance(offsets, torch.Tensor):
+        offsets = offsets.cpu().numpy()
+    offs = np.ascontiguousarray(np.asarray(offsets, dtype=np.int64)).astype(np.uint64)
+    if offs.ndim != 1 or offs.size < 1:
+        raise ValueError("offsets must hold num_segments + 1 entries")
+    if offs.size > 1 and int(offs[-1]) > n:
+        raise ValueError("offsets reach past the end of keys_in")
+    if keys_out is None:
+        keys_out = keys_in.clone()
+    _check_tensor(keys_out, n, "keys_out")
+    args = (kind, _ptr(keys_in), _ptr(keys_out), offs.size - 1, ctypes.c_void_p(offs.ctypes.data),
+            int(bool(descending)), _stream(stream))
+    temp = _run(load().gbs_segmented_sort_offsets, args, temp, "gbs_segmented_sort_offsets")
+    return (keys_out, temp) if return_temp else keys_out
 
 
 def gbs_digit_histograms(keys: torch.Tensor, begin_bit: int = 0, end_bit: int | None = None,

@@ -93,6 +93,31 @@ def test_host_entry_rejects_bad_arguments(lib):
         gbsort.GBS_ERR_INVALID_ARG
 
 
+def _offsets(values):
+    a = (ctypes.c_uint64 * len(values))(*values)
+    return a
+
+
+def test_segmented_offsets_temp_and_arguments(lib):
+    small = _offsets([0, 10, 10, 5000, 21384])  # longest 16384: bitonic only
+    st, need_small = _query(lib, "gbs_segmented_sort_offsets", gbsort.GBS_U32, None, None, 4, small, 0, None)
+    assert st == gbsort.GBS_OK and need_small < 4096
+    big = _offsets([0, 10, 100010, 100011])     # one segment of 10^5 keys: radix work area
+    st, need_big = _query(lib, "gbs_segmented_sort_offsets", gbsort.GBS_U32, None, None, 3, big, 0, None)
+    _, radix = _query(lib, "gbs_sort_keys", gbsort.GBS_U32, None, None, 100000, 0, 32, 0, None)
+    assert st == gbsort.GBS_OK and need_big >= radix
+    bad = _offsets([0, 10, 5, 20])
+    assert _query(lib, "gbs_segmented_sort_offsets", gbsort.GBS_U32, None, None, 3, bad, 0, None)[0] == \
+        gbsort.GBS_ERR_INVALID_ARG
+    assert _query(lib, "gbs_segmented_sort_offsets", gbsort.GBS_U32, None, None, 3, None, 0, None)[0] == \
+        gbsort.GBS_ERR_INVALID_ARG
+    huge = _offsets([0, gbsort.GBS_MAX_RADIX_KEYS + 1])
+    assert _query(lib, "gbs_segmented_sort_offsets", gbsort.GBS_U64, None, None, 1, huge, 0, None)[0] == \
+        gbsort.GBS_ERR_UNSUPPORTED
+    st, need0 = _query(lib, "gbs_segmented_sort_offsets", gbsort.GBS_F64, None, None, 0, None, 0, None)
+    assert st == gbsort.GBS_OK and need0 > 0
+
+
 @pytest.mark.parametrize("begin,end", [(-1, 8), (9, 8), (0, 33)])
 def test_bad_bit_range(lib, begin, end):
     st, _ = _query(lib, "gbs_sort_keys", gbsort.GBS_U32, None, None, 10, begin, end, 0, None)

@@ -238,6 +238,45 @@ def test_segmented_sort(g, dtype, seg_len):
         assert np.array_equal(_u(got), _u(oracle.segmented_sort(keys, segs, seg_len, descending=desc))), desc
 
 
+SEG_MIX = [0, 1, 2, 3, 5, 17, 100, 255, 256, 1000, 1023, 1024, 1025, 2047, 4097, 8191, 16383, 16384, 16385,
+           20000, 70001, 0, 7, 300, 3000]
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("desc", [False, True])
+@pytest.mark.parametrize("in_place", [False, True])
+def test_segmented_sort_offsets(g, dtype, desc, in_place):
+    # lengths of every class (0, 1, 2^l and its neighbours, past 2^14), a leading and a trailing gap
+    extra = (wl.uniform_u32(40, wl.seed_for(72, 1)) % np.uint32(600)).astype(np.int64)
+    lens = np.array(SEG_MIX + extra.tolist(), dtype=np.int64)
+    offs = np.concatenate([[7], 7 + np.cumsum(lens)])
+    n = int(offs[-1]) + 9
+    keys = with_ties(dtype, n, 73, k=5000) if desc else sample(dtype, n, 73)
+    tin = _dev(keys)
+    if in_place:
+        out = g.gbs_segmented_sort_offsets(tin, offs, keys_out=tin, descending=desc)
+    else:
+        out = g.gbs_segmented_sort_offsets(tin, offs, descending=desc)  # keys_out starts as a copy
+    got = _host(out)
+    u = _u
+    for s_, e_ in zip(offs[:-1], offs[1:]):
+        want = oracle.sort_keys(keys[s_:e_], descending=desc)
+        assert np.array_equal(u(got[s_:e_]), u(want)), (s_, e_ - s_)
+    assert np.array_equal(u(got[:7]), u(keys[:7])) and np.array_equal(u(got[offs[-1]:]), u(keys[offs[-1]:]))
+    if not in_place:
+        assert np.array_equal(u(_host(tin)), u(keys))
+
+
+def test_segmented_offsets_empty_and_status(g):
+    t = _dev(wl.uniform_u32(100, 3))
+    out, temp = g.gbs_segmented_sort_offsets(t, [0], return_temp=True)
+    assert g.gbs_get_status(temp) == g.GBS_OK
+    out, temp = g.gbs_segmented_sort_offsets(t, [10, 10, 10, 90], return_temp=True)
+    assert g.gbs_get_status(temp) == g.GBS_OK
+    h = _host(t)
+    assert np.array_equal(_host(out)[10:90], np.sort(h[10:90])) and np.array_equal(_host(out)[:10], h[:10])
+
+
 def test_segmented_zero_one_principle_exhaustive(g):
     # every 0-1 pattern of 16 keys, one per segment ("并行排序" §1.2, 0-1 principle)
     pats = wl.zero_one_patterns(16)
