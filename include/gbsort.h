@@ -128,6 +128,16 @@ gbs_status gbs_sort_pairs(void *d_temp, size_t *temp_bytes, gbs_key_type key_typ
                           int begin_bit, int end_bit, int descending, void *stream);
 
 /*
+ * gbs_sort_pairs64 — gbs_sort_pairs with one uint64_t value per key (for
+ * payloads such as 64-bit indices or pointers).  Stable.
+ *   d_vals_in / d_vals_out  device arrays of n uint64_t; may be equal
+ */
+gbs_status gbs_sort_pairs64(void *d_temp, size_t *temp_bytes, gbs_key_type key_type,
+                            const void *d_keys_in, void *d_keys_out,
+                            const uint64_t *d_vals_in, uint64_t *d_vals_out, size_t n,
+                            int begin_bit, int end_bit, int descending, void *stream);
+
+/*
  * gbs_segmented_sort — sort each of num_segments consecutive segments of
  * segment_len keys independently, over the full key width, with the bitonic
  * network ("并行排序" §3.3-3.5, §4.2-4.3).  A segment whose length is not a

@@ -38,8 +38,10 @@ void gbs_debug_set_timing_events(void **events, int count);
 /* Number of kernels the calling thread's last sorting call launched. */
 int gbs_debug_last_launch_count(void);
 
-/* Keys per tile of the radix pass kernel for a key width (4 or 8 bytes). */
-size_t gbs_debug_radix_tile_keys(int key_bytes, int pairs);
+/* Keys per tile of the radix pass kernel for a key width (4 or 8 bytes) and
+ * a value width (0: keys only; 8: 64-bit values; any other non-zero: 32-bit
+ * values). */
+size_t gbs_debug_radix_tile_keys(int key_bytes, int value_bytes);
 
 #ifdef __cplusplus
 }

@@ -52,9 +52,9 @@ struct Layout {
     uint32_t num_tiles;
 };
 
-Layout radix_layout(int key_bytes, bool pairs, size_t n) {
+Layout radix_layout(int key_bytes, int val_bytes, size_t n) {
     Layout l;
-    const uint32_t tile = gbs::radix_tile_keys(key_bytes, pairs);
+    const uint32_t tile = gbs::radix_tile_keys(key_bytes, val_bytes);
     l.num_tiles = (uint32_t)((n + tile - 1) / tile);
     size_t off = sizeof(Header);
     l.hist = off;
@@ -66,7 +66,7 @@ Layout radix_layout(int key_bytes, bool pairs, size_t n) {
     l.keys_alt = off;
     off += round_up((size_t)key_bytes * n);
     l.vals_alt = off;
-    if (pairs) off += round_up(sizeof(uint32_t) * n);
+    off += round_up((size_t)val_bytes * n);
     l.total = off;
     return l;
 }
@@ -93,16 +93,18 @@ cudaError_t copy_if_needed(const void *src, void *dst, size_t bytes, cudaStream_
 
 // keep_error: leave the header's error words as they are (a call made of
 // several sorts reports the first error of any of them).
+// val_bytes: 0 (keys only), 4 or 8 bytes per value.
 gbs_status radix_common(void *d_temp, size_t *temp_bytes, gbs_key_type kt, const void *keys_in, void *keys_out,
-                        const uint32_t *vals_in, uint32_t *vals_out, bool pairs, size_t n, int begin_bit,
-                        int end_bit, int descending, void *stream, bool keep_error = false) {
+                        const void *vals_in, void *vals_out, int val_bytes, size_t n, int begin_bit, int end_bit,
+                        int descending, void *stream, bool keep_error = false) {
+    const bool pairs = val_bytes != 0;
     if (!keep_error) t_launches = 0;
     const int kb = key_bytes_of(kt);
     if (kb == 0) return GBS_ERR_INVALID_ARG;
     if (temp_bytes == nullptr) return GBS_ERR_INVALID_ARG;
     if (begin_bit < 0 || end_bit < begin_bit || end_bit > 8 * kb) return GBS_ERR_INVALID_ARG;
     if (n > GBS_MAX_RADIX_KEYS) return GBS_ERR_UNSUPPORTED;
-    const Layout lay = radix_layout(kb, pairs, n);
+    const Layout lay = radix_layout(kb, val_bytes, n);
     bool query = false;
     gbs_status st = check_temp(d_temp, temp_bytes, lay.total, &query);
     if (st != GBS_OK || query) return st;
@@ -118,7 +120,7 @@ gbs_status radix_common(void *d_temp, size_t *temp_bytes, gbs_key_type kt, const
     const int passes = (end_bit - begin_bit + 7) / 8;
     if (n <= 1 || passes == 0) {
         e = copy_if_needed(keys_in, keys_out, n * kb, s);
-        if (e == cudaSuccess && pairs) e = copy_if_needed(vals_in, vals_out, n * 4, s);
+        if (e == cudaSuccess && pairs) e = copy_if_needed(vals_in, vals_out, n * (size_t)val_bytes, s);
         return from_cuda(e);
     }
     timing_start(s);
@@ -131,13 +133,13 @@ gbs_status radix_common(void *d_temp, size_t *temp_bytes, gbs_key_type kt, const
     gbs::RadixJob job;
     job.kind = (int)kt;
     job.key_bytes = kb;
-    job.pairs = pairs;
+    job.val_bytes = val_bytes;
     job.keys_in = keys_in;
     job.keys_out = keys_out;
     job.keys_alt = tb + lay.keys_alt;
     job.vals_in = vals_in;
     job.vals_out = vals_out;
-    job.vals_alt = pairs ? reinterpret_cast<uint32_t *>(tb + lay.vals_alt) : nullptr;
+    job.vals_alt = pairs ? static_cast<void *>(tb + lay.vals_alt) : nullptr;
     job.n = n;
     job.begin_bit = begin_bit;
     job.end_bit = end_bit;
@@ -174,7 +176,7 @@ extern "C" {
 
 gbs_status gbs_sort_keys(void *d_temp, size_t *temp_bytes, gbs_key_type key_type, const void *d_keys_in,
                          void *d_keys_out, size_t n, int begin_bit, int end_bit, int descending, void *stream) {
-    return radix_common(d_temp, temp_bytes, key_type, d_keys_in, d_keys_out, nullptr, nullptr, false, n, begin_bit,
+    return radix_common(d_temp, temp_bytes, key_type, d_keys_in, d_keys_out, nullptr, nullptr, 0, n, begin_bit,
                         end_bit, descending, stream);
 }
 
@@ -187,7 +189,7 @@ gbs_status gbs_sort_keys_host(void *d_temp, size_t *temp_bytes, gbs_key_type key
     // work buffer: the in-place device sort's own work buffer first (so that
     // gbs_get_status finds its header at d_temp), then the keys' device copy
     size_t sort_bytes = 0;
-    gbs_status st = radix_common(nullptr, &sort_bytes, key_type, nullptr, nullptr, nullptr, nullptr, false, n,
+    gbs_status st = radix_common(nullptr, &sort_bytes, key_type, nullptr, nullptr, nullptr, nullptr, 0, n,
                                  begin_bit, end_bit, descending, stream);
     if (st != GBS_OK) return st;
     const size_t keys_off = round_up(sort_bytes);
@@ -200,7 +202,7 @@ gbs_status gbs_sort_keys_host(void *d_temp, size_t *temp_bytes, gbs_key_type key
     if (n > 0 && cudaMemcpyAsync(d_keys, h_keys_in, n * kb, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return GBS_ERR_CUDA;
     size_t inner = keys_off;  // also clears the status header when n == 0
-    st = radix_common(d_temp, &inner, key_type, d_keys, d_keys, nullptr, nullptr, false, n, begin_bit, end_bit,
+    st = radix_common(d_temp, &inner, key_type, d_keys, d_keys, nullptr, nullptr, 0, n, begin_bit, end_bit,
                       descending, stream);
     if (st != GBS_OK || n == 0) return st;
     return from_cuda(cudaMemcpyAsync(h_keys_out, d_keys, n * kb, cudaMemcpyDeviceToHost, s));
@@ -209,7 +211,14 @@ gbs_status gbs_sort_keys_host(void *d_temp, size_t *temp_bytes, gbs_key_type key
 gbs_status gbs_sort_pairs(void *d_temp, size_t *temp_bytes, gbs_key_type key_type, const void *d_keys_in,
                           void *d_keys_out, const uint32_t *d_vals_in, uint32_t *d_vals_out, size_t n,
                           int begin_bit, int end_bit, int descending, void *stream) {
-    return radix_common(d_temp, temp_bytes, key_type, d_keys_in, d_keys_out, d_vals_in, d_vals_out, true, n,
+    return radix_common(d_temp, temp_bytes, key_type, d_keys_in, d_keys_out, d_vals_in, d_vals_out, 4, n,
+                        begin_bit, end_bit, descending, stream);
+}
+
+gbs_status gbs_sort_pairs64(void *d_temp, size_t *temp_bytes, gbs_key_type key_type, const void *d_keys_in,
+                            void *d_keys_out, const uint64_t *d_vals_in, uint64_t *d_vals_out, size_t n,
+                            int begin_bit, int end_bit, int descending, void *stream) {
+    return radix_common(d_temp, temp_bytes, key_type, d_keys_in, d_keys_out, d_vals_in, d_vals_out, 8, n,
                         begin_bit, end_bit, descending, stream);
 }
 
@@ -266,7 +275,7 @@ gbs_status gbs_segmented_sort_offsets(void *d_temp, size_t *temp_bytes, gbs_key_
     // work buffer: [radix work area, or just the status header][offsets][segment ids by class]
     size_t radix_bytes = sizeof(Header);
     if (longest > 0) {
-        gbs_status st = radix_common(nullptr, &radix_bytes, key_type, nullptr, nullptr, nullptr, nullptr, false,
+        gbs_status st = radix_common(nullptr, &radix_bytes, key_type, nullptr, nullptr, nullptr, nullptr, 0,
                                      longest, 0, 8 * kb, descending, stream);
         if (st != GBS_OK) return st;
     }
@@ -321,7 +330,7 @@ gbs_status gbs_segmented_sort_offsets(void *d_temp, size_t *temp_bytes, gbs_key_
         const size_t lo = h_offsets[id], len = h_offsets[id + 1] - lo;
         size_t have = radix_bytes;
         st = radix_common(d_temp, &have, key_type, static_cast<const unsigned char *>(d_keys_in) + lo * kb,
-                          static_cast<unsigned char *>(d_keys_out) + lo * kb, nullptr, nullptr, false, len, 0,
+                          static_cast<unsigned char *>(d_keys_out) + lo * kb, nullptr, nullptr, 0, len, 0,
                           8 * kb, descending, stream, /*keep_error=*/true);
         if (st != GBS_OK) return st;
     }
@@ -400,8 +409,8 @@ void gbs_debug_set_timing_events(void **events, int count) {
     t_event_count = events ? count : 0;
 }
 
-size_t gbs_debug_radix_tile_keys(int key_bytes, int pairs) {
-    return gbs::radix_tile_keys(key_bytes, pairs != 0);
+size_t gbs_debug_radix_tile_keys(int key_bytes, int value_bytes) {
+    return gbs::radix_tile_keys(key_bytes, value_bytes == 8 ? 8 : value_bytes ? 4 : 0);
 }
 
 }  // extern "C"

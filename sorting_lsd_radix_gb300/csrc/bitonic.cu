@@ -284,12 +284,10 @@ template <typename K, int L_LOG, int K_LOG>
 cudaError_t launch_shape(const BitonicParams &prm, cudaStream_t stream) {
     using Sh = Shape<K, L_LOG, K_LOG>;
     auto kern = bitonic_tile_kernel<K, L_LOG, K_LOG>;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sh::SMEM);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static PerDeviceOnce once;
+    const cudaError_t e =
+        once.run([&] { return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sh::SMEM); });
+    if (e != cudaSuccess) return e;
     const size_t grid = (prm.num_segments + Sh::SEGS - 1) / Sh::SEGS;
     kern<<<(unsigned)grid, Sh::T, Sh::SMEM, stream>>>(prm);
     return cudaGetLastError();

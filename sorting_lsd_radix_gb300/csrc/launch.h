@@ -1,6 +1,7 @@
 // Host-side interface between the C ABI (api.cu) and the kernel files.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -9,17 +10,38 @@
 
 namespace gbs {
 
+// One-time set-up of a kernel (its shared-memory attribute), done once per
+// device: the first launch on each device runs `setup`; a set-up that fails
+// is tried again on the next launch.  Devices 0..63 are remembered, others set
+// up on every launch.  Two threads may both run a set-up; it is idempotent.
+class PerDeviceOnce {
+  public:
+    template <typename F> cudaError_t run(F &&setup) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return setup();
+        const uint64_t bit = uint64_t(1) << dev;
+        if (done_.load(std::memory_order_acquire) & bit) return cudaSuccess;
+        const cudaError_t e = setup();
+        if (e == cudaSuccess) done_.fetch_or(bit, std::memory_order_acq_rel);
+        return e;
+    }
+
+  private:
+    std::atomic<uint64_t> done_{0};
+};
+
+
 // Everything one radix sort call needs on the device.
 struct RadixJob {
     int kind;             // KeyKind
     int key_bytes;        // 4 or 8
-    bool pairs;
+    int val_bytes;        // 0 (keys only), 4 or 8
     const void *keys_in;
     void *keys_out;
     void *keys_alt;       // n keys of scratch in the work buffer
-    const uint32_t *vals_in;
-    uint32_t *vals_out;
-    uint32_t *vals_alt;   // n values of scratch (pairs only)
+    const void *vals_in;  // values of val_bytes each
+    void *vals_out;
+    void *vals_alt;       // n values of scratch (pairs only)
     size_t n;
     int begin_bit, end_bit, num_passes;
     bool descending;
@@ -38,8 +60,9 @@ struct RadixJob {
 // caller-provided event on the stream after a launch, if the hook is set.
 void timing_mark(cudaStream_t stream);
 
-// Tile (keys per CTA) of the one-sweep pass kernel for a key width / pairs.
-uint32_t radix_tile_keys(int key_bytes, bool pairs);
+// Tile (keys per CTA) of the one-sweep pass kernel for a key width and a
+// value width (0: keys only).
+uint32_t radix_tile_keys(int key_bytes, int val_bytes);
 
 // Histogram + plan, then every digit pass (and the final copy when needed).
 cudaError_t launch_radix_sort(const RadixJob &job, cudaStream_t stream, int *launches);

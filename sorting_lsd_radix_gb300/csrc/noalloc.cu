@@ -71,7 +71,7 @@ extern "C" gbs_status gbs_sort_keys_noalloc(gbs_key_type key_type, const void *d
     if (st != GBS_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-    const uint32_t tile = gbs::radix_tile_keys(kb, false);
+    const uint32_t tile = gbs::radix_tile_keys(kb, 0);
     const uint32_t tiles = (uint32_t)((n + tile - 1) / tile);
     const size_t off_hist = kHeader, off_base = off_hist + kHist, off_status = off_base + kHist;
     const size_t off_keys = off_status + up((size_t)tiles * 256 * 4);
@@ -91,7 +91,7 @@ extern "C" gbs_status gbs_sort_keys_noalloc(gbs_key_type key_type, const void *d
     gbs::RadixJob job;
     job.kind = (int)key_type;
     job.key_bytes = kb;
-    job.pairs = false;
+    job.val_bytes = 0;
     job.keys_in = d_keys_in;
     job.keys_out = d_keys_out;
     job.keys_alt = scratch + off_keys;

@@ -11,6 +11,8 @@
 // digits, 16-byte vector loads); "并行排序：从归并网络到 GPU 双调排序" §8.1
 // (warp-level histograms, block-local sort before the global write).
 #include <algorithm>
+#include <atomic>
+#include <type_traits>
 
 #include "launch.h"
 
@@ -254,11 +256,14 @@ __global__ void __launch_bounds__(HIST_THREADS, 1) upfront_histogram_kernel(cons
 // One digit pass
 // ---------------------------------------------------------------------------
 
-template <typename K, bool PAIRS, int THREADS, int ITEMS> struct PassSmem {
+// Value type of a pass with VB value bytes per key (0: keys only).
+template <int VB> using ValueT = typename std::conditional<VB == 8, uint64_t, uint32_t>::type;
+
+template <typename K, int VB, int THREADS, int ITEMS> struct PassSmem {
     static constexpr int TILE = THREADS * ITEMS;
     static constexpr int WARPS = THREADS / 32;
     K keys[TILE];
-    uint32_t vals[PAIRS ? TILE : 4];
+    ValueT<VB> vals[VB ? TILE : 4];
     // per-warp digit counters; after the count phase: sorted-tile slot of the
     // warp's first key of each digit
     uint32_t whist[WARPS][256];
@@ -272,9 +277,9 @@ struct PassParams {
     const void *keys_in;
     void *keys_out;
     void *keys_alt;
-    const uint32_t *vals_in;
-    uint32_t *vals_out;
-    uint32_t *vals_alt;
+    const void *vals_in;  // ValueT<VB> arrays (unused when keys only)
+    void *vals_out;
+    void *vals_alt;
     uint32_t n;
     // order-preserving code of a key: x ^ ((x >>s (w-1)) & a) ^ b (code_consts)
     uint32_t enc_a, enc_b;
@@ -426,9 +431,9 @@ __device__ __forceinline__ void rank_warp(const K *tile_keys, uint32_t *whist, c
 
 // Coalesced scatter of the sorted tile: consecutive slots of one digit go to
 // consecutive global positions.  DEC applies the inverse key code (last pass).
-template <bool DEC, bool BYTE, typename K, bool PAIRS, int THREADS>
-__device__ __forceinline__ void store_tile(const K *sk, const uint32_t *sv, const uint32_t *binoff, uint32_t valid,
-                                           K *kdst, uint32_t *vdst, const PassParams &prm, int tid) {
+template <bool DEC, bool BYTE, typename K, int VB, int THREADS>
+__device__ __forceinline__ void store_tile(const K *sk, const ValueT<VB> *sv, const uint32_t *binoff, uint32_t valid,
+                                           K *kdst, ValueT<VB> *vdst, const PassParams &prm, int tid) {
 #pragma unroll 4
     for (uint32_t j = tid; j < valid; j += THREADS) {
         const K key = sk[j];
@@ -438,7 +443,7 @@ __device__ __forceinline__ void store_tile(const K *sk, const uint32_t *sv, cons
         // of the output
         if (pos < prm.n) {
             kdst[pos] = DEC ? Xform<K>::dec(key, prm) : key;
-            if (PAIRS) vdst[pos] = sv[j];
+            if (VB) vdst[pos] = sv[j];
         }
     }
 }
@@ -539,11 +544,12 @@ template <int WARPS> __device__ __forceinline__ uint32_t tile_digit_count(uint32
 // active pass lands in the output (or in the scratch buffer when an in-place
 // call has an odd number of active passes, which keeps every pass out of
 // place; the copy kernel then finishes).
-template <typename K, bool PAIRS> struct PassIO {
+template <typename K, int VB> struct PassIO {
+    using V = ValueT<VB>;
     const K *ksrc;
     K *kdst;
-    const uint32_t *vsrc = nullptr;
-    uint32_t *vdst = nullptr;
+    const V *vsrc = nullptr;
+    V *vdst = nullptr;
     __device__ __forceinline__ PassIO(const PassParams &prm, uint32_t A, uint32_t k) {
         const bool odd_in_place = prm.in_place && (A & 1u);
         K *kout = reinterpret_cast<K *>(prm.keys_out), *kalt = reinterpret_cast<K *>(prm.keys_alt);
@@ -551,10 +557,11 @@ template <typename K, bool PAIRS> struct PassIO {
         const bool src_last = ((A - k) & 1u) == 0, dst_last = ((A - 1 - k) & 1u) == 0;
         ksrc = (k == 0) ? reinterpret_cast<const K *>(prm.keys_in) : (src_last ? k_last : k_other);
         kdst = dst_last ? k_last : k_other;
-        if (PAIRS) {
-            uint32_t *v_last = odd_in_place ? prm.vals_alt : prm.vals_out;
-            uint32_t *v_other = odd_in_place ? prm.vals_out : prm.vals_alt;
-            vsrc = (k == 0) ? prm.vals_in : (src_last ? v_last : v_other);
+        if (VB) {
+            V *vout = reinterpret_cast<V *>(prm.vals_out), *valt = reinterpret_cast<V *>(prm.vals_alt);
+            V *v_last = odd_in_place ? valt : vout;
+            V *v_other = odd_in_place ? vout : valt;
+            vsrc = (k == 0) ? reinterpret_cast<const V *>(prm.vals_in) : (src_last ? v_last : v_other);
             vdst = dst_last ? v_last : v_other;
         }
     }
@@ -591,11 +598,26 @@ template <typename K, bool PAIRS> struct PassIO {
 #ifndef GBS_U64_PAIR_ITEMS
 #define GBS_U64_PAIR_ITEMS 12
 #endif
-template <typename K, bool PAIRS, int THREADS, int ITEMS, bool BYTE>
+// 64-bit values
+#ifndef GBS_U32_V64_THREADS
+#define GBS_U32_V64_THREADS 256
+#endif
+#ifndef GBS_U32_V64_ITEMS
+#define GBS_U32_V64_ITEMS 16
+#endif
+#ifndef GBS_U64_V64_THREADS
+#define GBS_U64_V64_THREADS 256
+#endif
+#ifndef GBS_U64_V64_ITEMS
+#define GBS_U64_V64_ITEMS 12
+#endif
+template <typename K, int VB, int THREADS, int ITEMS, bool BYTE>
 __global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
     onesweep_pass_kernel(const PassParams prm) {
+    constexpr bool PAIRS = VB != 0;
+    using V = ValueT<VB>;
     static_assert(THREADS * ITEMS <= 65536, "in-tile ranks are 16-bit");
-    using S = PassSmem<K, PAIRS, THREADS, ITEMS>;
+    using S = PassSmem<K, VB, THREADS, ITEMS>;
     constexpr int TILE = S::TILE;
     constexpr int WARPS = S::WARPS;
     // one thread per digit in the count, scan and look-back phases
@@ -615,7 +637,9 @@ __global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
             const size_t lo = (size_t)blockIdx.x * TILE, hi = min((size_t)prm.n, lo + TILE);
             copy_range(reinterpret_cast<const K *>(prm.keys_in), reinterpret_cast<K *>(prm.keys_out), lo, hi, tid,
                        THREADS);
-            if (PAIRS) copy_range(prm.vals_in, prm.vals_out, lo, hi, tid, THREADS);
+            if (PAIRS)
+                copy_range(reinterpret_cast<const V *>(prm.vals_in), reinterpret_cast<V *>(prm.vals_out), lo, hi, tid,
+                           THREADS);
         }
         return;
     }
@@ -624,17 +648,17 @@ __global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
     // the last one's store, unless it is the identity (unsigned ascending)
     const bool first = (k == 0) && !prm.identity, last = (k + 1 == A) && !prm.identity;
 
-    const PassIO<K, PAIRS> io(prm, A, k);
+    const PassIO<K, VB> io(prm, A, k);
     const K *ksrc = io.ksrc;
     K *kdst = io.kdst;
-    const uint32_t *vsrc = io.vsrc;
-    uint32_t *vdst = io.vdst;
+    const V *vsrc = io.vsrc;
+    V *vdst = io.vdst;
 
     // chained-scan states of this pass (rotated by ordinal, see common.cuh)
     const uint32_t st_agg = 1u + 2u * (k % 3u), st_inc = 2u + 2u * (k % 3u);
     const bool aligned = ((reinterpret_cast<uintptr_t>(ksrc) & 15) == 0) &&
                          (!PAIRS || ((reinterpret_cast<uintptr_t>(vsrc) & 15) == 0));
-    const uint32_t tx_bytes = TILE * (uint32_t)sizeof(K) + (PAIRS ? TILE * 4u : 0u);
+    const uint32_t tx_bytes = TILE * (uint32_t)(sizeof(K) + VB);
 
     // ---- ticket and tile load ---------------------------------------------
     // Tiles are taken in ticket order (forward progress of the look-back).
@@ -649,7 +673,7 @@ __global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
         if (spec_ok) {
             mbar_arrive_expect_tx(&sm.bar, tx_bytes);
             bulk_g2s(sm.keys, ksrc + (size_t)spec * TILE, TILE * (uint32_t)sizeof(K), &sm.bar);
-            if (PAIRS) bulk_g2s(sm.vals, vsrc + (size_t)spec * TILE, TILE * 4u, &sm.bar);
+            if (PAIRS) bulk_g2s(sm.vals, vsrc + (size_t)spec * TILE, TILE * (uint32_t)VB, &sm.bar);
         }
         sm.tile = atomicAdd(&hdr->tile_counter[prm.pass], 1u);
     }
@@ -675,7 +699,7 @@ __global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
                 if (tid == 0) {
                     mbar_arrive_expect_tx(&sm.bar, tx_bytes);
                     bulk_g2s(sm.keys, ksrc + tile_start, TILE * (uint32_t)sizeof(K), &sm.bar);
-                    if (PAIRS) bulk_g2s(sm.vals, vsrc + tile_start, TILE * 4u, &sm.bar);
+                    if (PAIRS) bulk_g2s(sm.vals, vsrc + tile_start, TILE * (uint32_t)VB, &sm.bar);
                 }
                 wait_phase(&sm.bar, phase, prm, hdr, tile);
             } else {
@@ -732,11 +756,11 @@ __global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
         }
     }
     if (PAIRS) {
-        uint32_t vals[ITEMS];
+        V vals[ITEMS];
 #pragma unroll
         for (int i = 0; i < ITEMS; ++i) {
             const uint32_t idx = (uint32_t)warp * (ITEMS * 32) + i * 32 + lane;
-            vals[i] = (idx < valid) ? sm.vals[idx] : 0u;
+            vals[i] = (idx < valid) ? sm.vals[idx] : V(0);
         }
         __syncthreads();
 #pragma unroll
@@ -764,9 +788,9 @@ __global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
     __syncthreads();
 
     if (last)
-        store_tile<true, BYTE, K, PAIRS, THREADS>(sm.keys, sm.vals, sm.binoff, valid, kdst, vdst, prm, tid);
+        store_tile<true, BYTE, K, VB, THREADS>(sm.keys, sm.vals, sm.binoff, valid, kdst, vdst, prm, tid);
     else
-        store_tile<false, BYTE, K, PAIRS, THREADS>(sm.keys, sm.vals, sm.binoff, valid, kdst, vdst, prm, tid);
+        store_tile<false, BYTE, K, VB, THREADS>(sm.keys, sm.vals, sm.binoff, valid, kdst, vdst, prm, tid);
 }
 
 // ---------------------------------------------------------------------------
@@ -777,9 +801,9 @@ struct CopyParams {
     const void *keys_in;
     void *keys_out;
     const void *keys_alt;
-    const uint32_t *vals_in;
-    uint32_t *vals_out;
-    const uint32_t *vals_alt;
+    const void *vals_in;
+    void *vals_out;
+    const void *vals_alt;
     size_t key_bytes_total;
     size_t val_bytes_total;
     const Header *hdr;
@@ -817,13 +841,16 @@ __global__ void __launch_bounds__(512) finish_copy_kernel(const CopyParams prm) 
 // Launch helpers
 // ---------------------------------------------------------------------------
 
+// SM count of the current device (cached per device).
 int device_sms() {
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (sms <= 0) sms = 1;
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+    int sms = (dev >= 0 && dev < 64) ? cache[dev].load(std::memory_order_relaxed) : 0;
+    if (sms <= 0) {
+        if (dev < 0 || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+            return 1;
+        if (dev < 64) cache[dev].store(sms, std::memory_order_relaxed);
     }
     return sms;
 }
@@ -852,16 +879,16 @@ cudaError_t launch_hist(const RadixJob &job, cudaStream_t stream, bool plan, int
     prm.zero_vec = plan ? (size_t)job.num_tiles * 256 * 4 / 16 : 0;
     prm.plan = plan ? 1 : 0;
     const bool full = job.begin_bit == 0 && job.end_bit == 8 * (int)sizeof(K);
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(upfront_histogram_kernel<K, true>,
+    static PerDeviceOnce once;
+    cudaError_t e = once.run([] {
+        cudaError_t r = cudaFuncSetAttribute(upfront_histogram_kernel<K, true>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hist_smem_bytes<K>());
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(upfront_histogram_kernel<K, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(upfront_histogram_kernel<K, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)hist_smem_bytes<K>());
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+        return r;
+    });
+    if (e != cudaSuccess) return e;
     const size_t per_cta = (size_t)HIST_THREADS * HIST_UNROLL * HistCfg<K>::PER_VEC;
     size_t grid = std::max<size_t>((job.n + per_cta - 1) / per_cta, (prm.zero_vec + HIST_THREADS - 1) / HIST_THREADS);
     grid = std::min<size_t>(grid, (size_t)device_sms());
@@ -877,22 +904,21 @@ cudaError_t launch_hist(const RadixJob &job, cudaStream_t stream, bool plan, int
 
 // One pass-kernel instantiation: the one-time shared-memory attribute set-up
 // and the launch of one CTA per tile.
-template <typename K, bool PAIRS, int THREADS, int ITEMS, bool BYTE> struct PassLaunch {
-    using S = PassSmem<K, PAIRS, THREADS, ITEMS>;
+template <typename K, int VB, int THREADS, int ITEMS, bool BYTE> struct PassLaunch {
+    using S = PassSmem<K, VB, THREADS, ITEMS>;
     static cudaError_t launch(uint32_t num_tiles, const PassParams &prm, cudaStream_t stream) {
-        static bool configured = false;
-        if (!configured) {
-            cudaError_t e = cudaFuncSetAttribute(onesweep_pass_kernel<K, PAIRS, THREADS, ITEMS, BYTE>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(S));
-            if (e != cudaSuccess) return e;
-            configured = true;
-        }
-        onesweep_pass_kernel<K, PAIRS, THREADS, ITEMS, BYTE><<<num_tiles, THREADS, sizeof(S), stream>>>(prm);
+        static PerDeviceOnce once;
+        const cudaError_t e = once.run([] {
+            return cudaFuncSetAttribute(onesweep_pass_kernel<K, VB, THREADS, ITEMS, BYTE>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(S));
+        });
+        if (e != cudaSuccess) return e;
+        onesweep_pass_kernel<K, VB, THREADS, ITEMS, BYTE><<<num_tiles, THREADS, sizeof(S), stream>>>(prm);
         return cudaGetLastError();
     }
 };
 
-template <typename K, bool PAIRS, int THREADS, int ITEMS>
+template <typename K, int VB, int THREADS, int ITEMS>
 cudaError_t launch_passes(const RadixJob &job, cudaStream_t stream, int *launches) {
     const bool byte_digits = (job.begin_bit % 8) == 0;
     PassParams prm;
@@ -928,8 +954,8 @@ cudaError_t launch_passes(const RadixJob &job, cudaStream_t stream, int *launche
         prm.perm_sel = 0x4440u | (uint32_t)((prm.shift & 31) >> 3);
         const cudaError_t e =
             (byte_digits && bits == 8)
-                ? PassLaunch<K, PAIRS, THREADS, ITEMS, true>::launch(job.num_tiles, prm, stream)
-                : PassLaunch<K, PAIRS, THREADS, ITEMS, false>::launch(job.num_tiles, prm, stream);
+                ? PassLaunch<K, VB, THREADS, ITEMS, true>::launch(job.num_tiles, prm, stream)
+                : PassLaunch<K, VB, THREADS, ITEMS, false>::launch(job.num_tiles, prm, stream);
         if (e != cudaSuccess) return e;
         ++*launches;
         timing_mark(stream);
@@ -940,10 +966,15 @@ cudaError_t launch_passes(const RadixJob &job, cudaStream_t stream, int *launche
 }  // namespace
 
 // Keys per tile of each launch shape (the pass kernel's tuning macros).
-uint32_t radix_tile_keys(int key_bytes, bool pairs) {
-    if (key_bytes == 8) return pairs ? (uint32_t)GBS_U64_PAIR_THREADS * GBS_U64_PAIR_ITEMS
-                                     : (uint32_t)GBS_U64_THREADS * GBS_U64_ITEMS;
-    return pairs ? (uint32_t)GBS_U32_PAIR_THREADS * GBS_U32_PAIR_ITEMS : (uint32_t)GBS_U32_THREADS * GBS_U32_ITEMS;
+uint32_t radix_tile_keys(int key_bytes, int val_bytes) {
+    if (key_bytes == 8) {
+        if (val_bytes == 8) return (uint32_t)GBS_U64_V64_THREADS * GBS_U64_V64_ITEMS;
+        return val_bytes ? (uint32_t)GBS_U64_PAIR_THREADS * GBS_U64_PAIR_ITEMS
+                         : (uint32_t)GBS_U64_THREADS * GBS_U64_ITEMS;
+    }
+    if (val_bytes == 8) return (uint32_t)GBS_U32_V64_THREADS * GBS_U32_V64_ITEMS;
+    return val_bytes ? (uint32_t)GBS_U32_PAIR_THREADS * GBS_U32_PAIR_ITEMS
+                     : (uint32_t)GBS_U32_THREADS * GBS_U32_ITEMS;
 }
 
 cudaError_t launch_histograms(const RadixJob &job, cudaStream_t stream, int *launches) {
@@ -956,13 +987,15 @@ cudaError_t launch_radix_sort(const RadixJob &job, cudaStream_t stream, int *lau
     if (job.key_bytes == 8) {
         e = launch_hist<uint64_t>(job, stream, true, launches);
         if (e != cudaSuccess) return e;
-        e = job.pairs ? launch_passes<uint64_t, true, GBS_U64_PAIR_THREADS, GBS_U64_PAIR_ITEMS>(job, stream, launches)
-                      : launch_passes<uint64_t, false, GBS_U64_THREADS, GBS_U64_ITEMS>(job, stream, launches);
+        e = job.val_bytes == 8 ? launch_passes<uint64_t, 8, GBS_U64_V64_THREADS, GBS_U64_V64_ITEMS>(job, stream, launches)
+            : job.val_bytes    ? launch_passes<uint64_t, 4, GBS_U64_PAIR_THREADS, GBS_U64_PAIR_ITEMS>(job, stream, launches)
+                               : launch_passes<uint64_t, 0, GBS_U64_THREADS, GBS_U64_ITEMS>(job, stream, launches);
     } else {
         e = launch_hist<uint32_t>(job, stream, true, launches);
         if (e != cudaSuccess) return e;
-        e = job.pairs ? launch_passes<uint32_t, true, GBS_U32_PAIR_THREADS, GBS_U32_PAIR_ITEMS>(job, stream, launches)
-                      : launch_passes<uint32_t, false, GBS_U32_THREADS, GBS_U32_ITEMS>(job, stream, launches);
+        e = job.val_bytes == 8 ? launch_passes<uint32_t, 8, GBS_U32_V64_THREADS, GBS_U32_V64_ITEMS>(job, stream, launches)
+            : job.val_bytes    ? launch_passes<uint32_t, 4, GBS_U32_PAIR_THREADS, GBS_U32_PAIR_ITEMS>(job, stream, launches)
+                               : launch_passes<uint32_t, 0, GBS_U32_THREADS, GBS_U32_ITEMS>(job, stream, launches);
     }
     if (e != cudaSuccess) return e;
     if (job.in_place) {
@@ -971,10 +1004,10 @@ cudaError_t launch_radix_sort(const RadixJob &job, cudaStream_t stream, int *lau
         cp.keys_out = job.keys_out;
         cp.keys_alt = job.keys_alt;
         cp.vals_in = job.vals_in;
-        cp.vals_out = job.pairs ? job.vals_out : nullptr;
+        cp.vals_out = job.val_bytes ? job.vals_out : nullptr;
         cp.vals_alt = job.vals_alt;
         cp.key_bytes_total = job.n * (size_t)job.key_bytes;
-        cp.val_bytes_total = job.pairs ? job.n * 4 : 0;
+        cp.val_bytes_total = job.n * (size_t)job.val_bytes;
         cp.hdr = job.hdr;
         const size_t blocks = std::min<size_t>((cp.key_bytes_total / 16 + 511) / 512 + 1, (size_t)device_sms() * 4);
         finish_copy_kernel<<<(unsigned)blocks, 512, 0, stream>>>(cp);

@@ -39,7 +39,7 @@ _KIND_BYTES = {GBS_U32: 4, GBS_I32: 4, GBS_F32: 4, GBS_U64: 8, GBS_I64: 8, GBS_F
 EXPORTS = ("gbs_sort_keys", "gbs_sort_pairs", "gbs_segmented_sort", "gbs_digit_histograms", "gbs_get_status",
            "gbs_status_string", "gbs_version", "gbs_debug_set_lookback_fault", "gbs_debug_last_launch_count",
            "gbs_debug_radix_tile_keys", "gbs_debug_set_timing_events", "gbs_sort_keys_noalloc",
-           "gbs_sort_keys_host", "gbs_segmented_sort_offsets")
+           "gbs_sort_keys_host", "gbs_segmented_sort_offsets", "gbs_sort_pairs64")
 GBS_NOALLOC_MAX_KEYS = 1 << 20
 
 
@@ -68,6 +68,8 @@ def load(path: str | None = None):
     lib.gbs_sort_keys_host.argtypes = [vp, szp, i, vp, vp, sz, i, i, i, vp]
     lib.gbs_sort_keys_host.restype = i
     lib.gbs_sort_pairs.argtypes = [vp, szp, i, vp, vp, vp, vp, sz, i, i, i, vp]
+    lib.gbs_sort_pairs64.argtypes = [vp, szp, i, vp, vp, vp, vp, sz, i, i, i, vp]
+    lib.gbs_sort_pairs64.restype = i
     lib.gbs_sort_pairs.restype = i
     lib.gbs_segmented_sort_offsets.argtypes = [vp, szp, i, vp, vp, sz, vp, i, vp]
     lib.gbs_segmented_sort_offsets.restype = i
@@ -205,13 +207,13 @@ def gbs_sort_pairs(keys_in: torch.Tensor, vals_in: torch.Tensor, keys_out: torch
                    vals_out: torch.Tensor | None = None, begin_bit: int = 0, end_bit: int | None = None,
                    descending: bool = False, temp: torch.Tensor | None = None, key_type: int | None = None,
                    stream=None, return_temp: bool = False):
-    """Stable LSD radix sort of (key, uint32 value) pairs; returns (keys_out, vals_out)."""
+    """Stable LSD radix sort of (key, value) pairs with 4- or 8-byte values; returns (keys_out, vals_out)."""
     kind = _kind(keys_in, key_type)
     n = keys_in.numel()
     _check_tensor(keys_in, n, "keys_in")
     _check_tensor(vals_in, n, "vals_in")
-    if vals_in.element_size() != 4:
-        raise ValueError("values must be 4-byte elements")
+    if vals_in.element_size() not in (4, 8):
+        raise ValueError("values must be 4- or 8-byte elements")
     if keys_out is None:
         keys_out = torch.empty_like(keys_in)
     if vals_out is None:
@@ -222,7 +224,8 @@ def gbs_sort_pairs(keys_in: torch.Tensor, vals_in: torch.Tensor, keys_out: torch
         end_bit = 8 * _KIND_BYTES[kind]
     args = (kind, _ptr(keys_in), _ptr(keys_out), _ptr(vals_in), _ptr(vals_out), n, begin_bit, end_bit,
             int(bool(descending)), _stream(stream))
-    temp = _run(load().gbs_sort_pairs, args, temp, "gbs_sort_pairs")
+    fn = load().gbs_sort_pairs64 if vals_in.element_size() == 8 else load().gbs_sort_pairs
+    temp = _run(fn, args, temp, "gbs_sort_pairs")
     return (keys_out, vals_out, temp) if return_temp else (keys_out, vals_out)
 
 
@@ -339,5 +342,7 @@ def gbs_debug_set_timing_events(events) -> None:
     load().gbs_debug_set_timing_events(arr, len(events))
 
 
-def gbs_debug_radix_tile_keys(key_bytes: int, pairs: bool = False) -> int:
-    return load().gbs_debug_radix_tile_keys(key_bytes, int(bool(pairs)))
+def gbs_debug_radix_tile_keys(key_bytes: int, pairs: bool = False, value_bytes: int | None = None) -> int:
+    """Keys per radix tile; value_bytes (0, 4 or 8) overrides pairs (4-byte values)."""
+    vb = value_bytes if value_bytes is not None else (4 if pairs else 0)
+    return load().gbs_debug_radix_tile_keys(key_bytes, vb)

@@ -60,6 +60,9 @@ def test_temp_query_sizes(lib):
     assert need < 256 + 2 * 8 * 256 * 4 + tiles * 1024 + 4 * n + 4 * 256
     st2, need2 = _query(lib, "gbs_sort_pairs", gbsort.GBS_U64, None, None, None, None, n, 0, 64, 0, None)
     assert st2 == gbsort.GBS_OK and need2 >= 8 * n + 4 * n
+    st5, need5 = _query(lib, "gbs_sort_pairs64", gbsort.GBS_U32, None, None, None, None, n, 0, 32, 0, None)
+    assert st5 == gbsort.GBS_OK and need5 >= 4 * n + 8 * n
+    assert gbsort.gbs_debug_radix_tile_keys(4, value_bytes=8) * 12 <= 64 * 1024  # 64-bit value tile fits
     for kt in (gbsort.GBS_I64, gbsort.GBS_F64):
         st4, need4 = _query(lib, "gbs_sort_keys", kt, None, None, n, 0, 64, 1, None)
         assert st4 == gbsort.GBS_OK and need4 >= 8 * n

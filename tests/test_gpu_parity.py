@@ -115,6 +115,32 @@ BIT_RANGES = {np.uint32: [(0, 16), (3, 29), (8, 9), (0, 1), (31, 32), (5, 5), (1
 
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("desc", [False, True])
+@pytest.mark.parametrize("n", [3, 1000, 4097, 16385, 3 * TILE32 + 13])
+def test_sort_pairs64_stable(g, dtype, desc, n):
+    # 64-bit values follow the oracle's stable permutation (the oracle sorts (key, index) pairs)
+    keys = with_ties(dtype, n, n + 3)
+    vals = wl.uniform_u64(n, wl.seed_for(74, n))
+    _, order = oracle.sort_pairs(keys, np.arange(n, dtype=np.uint32), descending=desc)
+    ko, vo = g.gbs_sort_pairs(_dev(keys), _dev(vals), descending=desc)
+    assert np.array_equal(_u(_host(ko)), _u(keys[order.astype(np.int64)]))
+    assert np.array_equal(_host(vo), vals[order.astype(np.int64)])
+
+
+@pytest.mark.parametrize("dtype", [np.uint32, np.uint64])
+@pytest.mark.parametrize("bits", [(0, 16), (8, 8), (4, 28)])
+def test_sort_pairs64_in_place_bit_ranges(g, dtype, bits):
+    n = 2 * TILE32 + 77
+    keys = with_ties(dtype, n, 19, k=500)
+    vals = wl.uniform_u64(n, wl.seed_for(75, 1))
+    _, order = oracle.sort_pairs(keys, np.arange(n, dtype=np.uint32), bits[0], bits[1])
+    tk, tv = _dev(keys), _dev(vals)
+    g.gbs_sort_pairs(tk, tv, keys_out=tk, vals_out=tv, begin_bit=bits[0], end_bit=bits[1])
+    assert np.array_equal(_host(tk), keys[order.astype(np.int64)])
+    assert np.array_equal(_host(tv), vals[order.astype(np.int64)])
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("desc", [False, True])
 def test_partial_bit_ranges_pairs(g, dtype, desc):
     n = 3 * TILE32 + 11
     keys = sample(dtype, n, 5)
