@@ -431,10 +431,14 @@ __device__ __forceinline__ void rank_warp(const K *tile_keys, uint32_t *whist, c
 
 // Coalesced scatter of the sorted tile: consecutive slots of one digit go to
 // consecutive global positions.  DEC applies the inverse key code (last pass).
+#ifndef GBS_STORE_UNROLL
+#define GBS_STORE_UNROLL 4
+#endif
+constexpr int STORE_UNROLL = GBS_STORE_UNROLL;
 template <bool DEC, bool BYTE, typename K, int VB, int THREADS>
 __device__ __forceinline__ void store_tile(const K *sk, const ValueT<VB> *sv, const uint32_t *binoff, uint32_t valid,
                                            K *kdst, ValueT<VB> *vdst, const PassParams &prm, int tid) {
-#pragma unroll 4
+#pragma unroll STORE_UNROLL
     for (uint32_t j = tid; j < valid; j += THREADS) {
         const K key = sk[j];
         const uint32_t pos = binoff[pass_digit<BYTE>(key, prm)] + j;
