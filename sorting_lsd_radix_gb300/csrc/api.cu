@@ -292,8 +292,10 @@ gbs_status gbs_segmented_sort_offsets(void *d_temp, size_t *temp_bytes, gbs_key_
     unsigned char *tb = reinterpret_cast<unsigned char *>(d_temp);
     if (cudaMemsetAsync(tb, 0, sizeof(Header), s) != cudaSuccess) return GBS_ERR_CUDA;
     if (num_segments == 0) return GBS_OK;
-    // segment ids grouped by class (host staging, copied with the offsets)
-    std::vector<uint32_t> ids(num_segments);
+    // host staging of one copy: the offsets, then the segment ids grouped by class
+    std::vector<unsigned char> staging(off_ids - off_offsets + sizeof(uint32_t) * num_segments);
+    std::memcpy(staging.data(), h_offsets, sizeof(uint64_t) * (num_segments + 1));
+    uint32_t *ids = reinterpret_cast<uint32_t *>(staging.data() + (off_ids - off_offsets));
     size_t start[CLASSES + 1] = {};
     for (int c = 1; c < CLASSES; ++c) start[c + 1] = start[c] + count[c];
     std::vector<uint32_t> long_ids;
@@ -314,10 +316,8 @@ gbs_status gbs_segmented_sort_offsets(void *d_temp, size_t *temp_bytes, gbs_key_
     }
     uint64_t *d_offsets = reinterpret_cast<uint64_t *>(tb + off_offsets);
     uint32_t *d_ids = reinterpret_cast<uint32_t *>(tb + off_ids);
-    // pageable sources: the copies are staged before these calls return
-    if (cudaMemcpyAsync(d_offsets, h_offsets, sizeof(uint64_t) * (num_segments + 1), cudaMemcpyHostToDevice, s) !=
-            cudaSuccess ||
-        cudaMemcpyAsync(d_ids, ids.data(), sizeof(uint32_t) * num_segments, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    // pageable source: the copy is staged before this call returns
+    if (cudaMemcpyAsync(d_offsets, staging.data(), staging.size(), cudaMemcpyHostToDevice, s) != cudaSuccess)
         return GBS_ERR_CUDA;
     timing_start(s);
     for (int c = 1; c < CLASSES; ++c) {

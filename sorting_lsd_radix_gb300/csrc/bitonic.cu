@@ -216,7 +216,26 @@ __global__ void __launch_bounds__(Shape<K, L_LOG, K_LOG>::T, (bitonic_min_blocks
     const bool vec = !listed && Sh::L % VEC == 0 && len == (uint32_t)Sh::L && seg0 + Sh::SEGS <= prm.num_segments &&
                      ((reinterpret_cast<uintptr_t>(in + seg0 * len) | reinterpret_cast<uintptr_t>(out + seg0 * len)) &
                       15) == 0;
-    if (listed) {
+    if (listed && Sh::L >= VEC) {
+        // VEC keys per step: one 16-byte load where the segment starts on a
+        // 16-byte boundary and the step lies inside it, else key by key
+        for (int e = tid; e < Sh::SEGS * Sh::L / VEC; e += Sh::T) {
+            const int k0 = e * VEC, s = k0 >> L_LOG, i = k0 & (Sh::L - 1);
+            const uint32_t len_s = s_len[s];
+            const K *src = in + s_base[s] + i;
+            K *dst = sm + s * Sh::LP + padded<Sh::PAD>(i);
+            if ((uint32_t)i + VEC <= len_s && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+                const uint4 w = __ldcs(reinterpret_cast<const uint4 *>(src));
+                const K *ks = reinterpret_cast<const K *>(&w);
+#pragma unroll
+                for (int u = 0; u < VEC; ++u) dst[u] = KeyCodec<K>::enc(ks[u], prm.kind, flip);
+            } else {
+#pragma unroll
+                for (int u = 0; u < VEC; ++u)
+                    dst[u] = ((uint32_t)i + u < len_s) ? KeyCodec<K>::enc(src[u], prm.kind, flip) : KeyCodec<K>::ALL_ONES;
+            }
+        }
+    } else if (listed) {
         for (int e = tid; e < Sh::SEGS * Sh::L; e += Sh::T) {
             const int s = e >> L_LOG, i = e & (Sh::L - 1);
             K v = KeyCodec<K>::ALL_ONES;
@@ -253,7 +272,26 @@ __global__ void __launch_bounds__(Shape<K, L_LOG, K_LOG>::T, (bitonic_min_blocks
 #pragma unroll
     for (int r = 0; r < Sh::KP; ++r) row[padded<Sh::PAD>(layout_index<K_LOG>(t, r, 0))] = x[r];
     __syncthreads();
-    if (listed) {
+    if (listed && Sh::L >= VEC) {
+        for (int e = tid; e < Sh::SEGS * Sh::L / VEC; e += Sh::T) {
+            const int k0 = e * VEC, s = k0 >> L_LOG, i = k0 & (Sh::L - 1);
+            const uint32_t len_s = s_len[s];
+            if ((uint32_t)i >= len_s) continue;
+            K *dstg = out + s_base[s] + i;
+            const K *src = sm + s * Sh::LP + padded<Sh::PAD>(i);
+            if ((uint32_t)i + VEC <= len_s && (reinterpret_cast<uintptr_t>(dstg) & 15) == 0) {
+                uint4 w;
+                K *ks = reinterpret_cast<K *>(&w);
+#pragma unroll
+                for (int u = 0; u < VEC; ++u) ks[u] = KeyCodec<K>::dec(src[u], prm.kind, flip);
+                __stcs(reinterpret_cast<uint4 *>(dstg), w);
+            } else {
+#pragma unroll
+                for (int u = 0; u < VEC; ++u)
+                    if ((uint32_t)i + u < len_s) dstg[u] = KeyCodec<K>::dec(src[u], prm.kind, flip);
+            }
+        }
+    } else if (listed) {
         for (int e = tid; e < Sh::SEGS * Sh::L; e += Sh::T) {
             const int s = e >> L_LOG, i = e & (Sh::L - 1);
             if ((uint32_t)i < s_len[s])

@@ -140,13 +140,20 @@ def _check_tensor(t: torch.Tensor, n: int, what: str):
 
 
 def _run(fn, args_after_temp, temp: torch.Tensor | None, what: str) -> torch.Tensor:
-    """Work-buffer protocol: query the size, (re)allocate with torch if needed, then run."""
+    """Work-buffer protocol: with a work buffer, run at once; without one, or if it is too small
+    (GBS_ERR_TEMP_TOO_SMALL, nothing launched), query the size, allocate with torch and run."""
+    if temp is not None:
+        have = ctypes.c_size_t(temp.numel())
+        st = fn(_ptr(temp), ctypes.byref(have), *args_after_temp)
+        if st == GBS_OK:
+            return temp
+        if st != GBS_ERR_TEMP_TOO_SMALL:
+            raise GbsError(st, what)
     need = ctypes.c_size_t(0)
     st = fn(None, ctypes.byref(need), *args_after_temp)
     if st != GBS_OK:
         raise GbsError(st, what)
-    if temp is None or temp.numel() < need.value:
-        temp = torch.empty(max(need.value, 256), dtype=torch.uint8, device="cuda")
+    temp = torch.empty(max(need.value, 256), dtype=torch.uint8, device="cuda")
     have = ctypes.c_size_t(temp.numel())
     st = fn(_ptr(temp), ctypes.byref(have), *args_after_temp)
     if st != GBS_OK:

@@ -238,6 +238,30 @@ def test_unaligned_pointers_use_plain_loads(g):
     assert np.array_equal(_host(out), oracle.sort_keys(base[1:], 0, 24))
 
 
+def test_concurrent_streams_with_separate_work_buffers(g):
+    # independent calls on two streams overlap on the GPU; each has its own work buffer
+    n1, n2 = 3 * TILE32 + 101, 5 * TILE64 + 7
+    k1 = sample(np.uint32, n1, 301)
+    k2 = sample(np.float64, n2, 302)
+    v1 = np.arange(n1, dtype=np.uint32)
+    d1, d2, dv1 = _dev(k1), _dev(k2), _dev(v1)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s1):
+        o1, ov1, t1 = g.gbs_sort_pairs(d1, dv1, descending=True, return_temp=True, stream=s1)
+    with torch.cuda.stream(s2):
+        o2, t2 = g.gbs_sort_keys(d2, return_temp=True, stream=s2)
+    for _ in range(5):
+        g.gbs_sort_pairs(d1, dv1, keys_out=o1, vals_out=ov1, descending=True, temp=t1, stream=s1)
+        g.gbs_sort_keys(d2, keys_out=o2, temp=t2, stream=s2)
+    s1.synchronize()
+    s2.synchronize()
+    ek, ev = oracle.sort_pairs(k1, v1, descending=True)
+    assert np.array_equal(_host(o1), ek) and np.array_equal(_host(ov1), ev)
+    assert np.array_equal(_u(_host(o2)), _u(oracle.sort_keys(k2)))
+    assert g.gbs_get_status(t1, stream=s1) == g.GBS_OK and g.gbs_get_status(t2, stream=s2) == g.GBS_OK
+
+
 def test_temp_reuse_across_calls(g):
     n = 100000
     a = wl.uniform_u32(n, 11)
