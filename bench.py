@@ -412,6 +412,8 @@ def _sec_segmented_var(num_segments, max_len):
 
 
 SECONDARY = {
+    "u32_2p20": ("sort_keys u32 n=2^20 uniform (L2-resident: launch-latency bound, roofline not meaningful)",
+                 _sec_radix_keys(lambda n: wl.uniform_u32(n, wl.seed_for(1, 0)), 1 << 20, "u32")),
     "u32_1e8_low_entropy": ("sort_keys u32 n=1e8, AND of three uniform draws",
                             _sec_radix_keys(lambda n: wl.low_entropy_u32(n, wl.seed_for(3, 1)), N_KEYS, "u32")),
     "u32_1e8_sorted": ("sort_keys u32 n=1e8, already ascending",
