@@ -1,6 +1,6 @@
 // LSD radix sort kernels (8-bit digits): the upfront digit histograms with
 // the device-side pass plan, the one-sweep digit pass (tile load, stable
-// warp-match rank, chained scan with decoupled look-back, shared-memory
+// ballot warp rank, chained scan with decoupled look-back, shared-memory
 // staged scatter) and the final copy.
 //
 // Method: kwkr.cn notes on bitonic vs LSD radix sort §3.1-3.2 (count, exclusive
