@@ -262,6 +262,36 @@ def test_concurrent_streams_with_separate_work_buffers(g):
     assert g.gbs_get_status(t1, stream=s1) == g.GBS_OK and g.gbs_get_status(t2, stream=s2) == g.GBS_OK
 
 
+@pytest.mark.parametrize("n", [5000, 3 * TILE32 + 5])
+def test_sort_captured_in_cuda_graph(g, n):
+    # every entry point only enqueues work on the stream, so a call can be captured once and
+    # replayed on new contents of the same buffers
+    d_in = _dev(sample(np.uint32, n, 401))
+    d_out = torch.empty_like(d_in)
+    v_in = _dev(np.arange(n, dtype=np.uint32))
+    v_out = torch.empty_like(v_in)
+    _, temp = g.gbs_sort_keys(d_in, keys_out=d_out, return_temp=True)           # warm-up: kernel set-up
+    _, _, ptemp = g.gbs_sort_pairs(d_in, v_in, keys_out=d_out, vals_out=v_out, descending=True, return_temp=True)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        g.gbs_sort_keys(d_in, keys_out=d_out, temp=temp)
+    pgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(pgraph):
+        g.gbs_sort_pairs(d_in, v_in, keys_out=d_out, vals_out=v_out, descending=True, temp=ptemp)
+    for seed in (402, 403):
+        keys = with_ties(np.uint32, n, seed)
+        d_in.copy_(_dev(keys))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(_host(d_out), oracle.sort_keys(keys))
+        pgraph.replay()
+        torch.cuda.synchronize()
+        ek, ev = oracle.sort_pairs(keys, np.arange(n, dtype=np.uint32), descending=True)
+        assert np.array_equal(_host(d_out), ek) and np.array_equal(_host(v_out), ev)
+    assert g.gbs_get_status(temp) == g.GBS_OK and g.gbs_get_status(ptemp) == g.GBS_OK
+
+
 def test_temp_reuse_across_calls(g):
     n = 100000
     a = wl.uniform_u32(n, 11)
