@@ -111,3 +111,13 @@ def test_config5_2p28(g, kind, desc):
     del d, out, temp
     torch.cuda.empty_cache()
     assert np.array_equal(_u(got), _u(oracle.sort_keys(keys, descending=desc)))
+
+
+@pytest.mark.parametrize("dist", ["uniform", "all_equal"])
+def test_largest_accepted_size_u32(g, dist):
+    # GBS_MAX_RADIX_KEYS keys: the tile status words' 29-bit counts reach their limit (all-equal keys
+    # put every key in one digit; uniform keys make the largest prefixes near n)
+    n = g.GBS_MAX_RADIX_KEYS
+    keys = wl.uniform_u32(n, wl.seed_for(3, 7)) if dist == "uniform" else wl.all_equal_u32(n, wl.seed_for(3, 8))
+    got = _sorted_u32(g, keys)
+    assert np.array_equal(got, oracle.sort_keys(keys))
