@@ -348,8 +348,9 @@ def _active_passes(keys, begin, end):
     return act
 
 
-def _sec_radix_keys(gen, n, key_type, begin=0, end=None, desc=False):
-    def build(gbsort, torch):
+def _sec_radix_keys(gen, n_default, key_type, begin=0, end=None, desc=False):
+    def build(gbsort, torch, n=None):
+        n = n or n_default
         keys = gen(n)
         d = torch.from_numpy(keys).cuda()
         o = torch.empty_like(d)
@@ -469,7 +470,11 @@ def run_secondary(args):
     gbuild.build()
     from sorting_lsd_radix_gb300 import gbsort
     desc, builder = SECONDARY[args.workload]
-    call, temp, n, alg_bytes, dom_bytes, dom_idx, extra = builder(gbsort, torch)
+    # --n resizes the radix-sort workloads (a small case of the same distribution, e.g. for ncu)
+    if args.n != N_KEYS and "n" in builder.__code__.co_varnames[:builder.__code__.co_argcount]:
+        call, temp, n, alg_bytes, dom_bytes, dom_idx, extra = builder(gbsort, torch, args.n)
+    else:
+        call, temp, n, alg_bytes, dom_bytes, dom_idx, extra = builder(gbsort, torch)
     torch.cuda.synchronize()
     # a replayed CUDA graph bypasses the library's per-kernel timing hook: time whole calls only
     launches = 0 if extra.get("graph") else gbsort.gbs_debug_last_launch_count()
