@@ -62,6 +62,23 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+NOMINAL_HBM_GBS = 2 * 3996e6 * 8192 / 8 / 1e9  # 3996 MHz double data rate on an 8192-bit bus
+
+
+def theoretical_hbm_gbs():
+    """Pin-rate bound of the HBM: 2 x memory clock x bus width, from the device's own
+    attributes where torch exposes them, else the nominal GB300 figures."""
+    try:
+        import torch
+        pr = torch.cuda.get_device_properties(torch.cuda.current_device())
+        gbs = 2.0 * pr.memory_clock_rate * 1e3 * pr.memory_bus_width / 8 / 1e9
+        if 1000.0 < gbs < 20000.0:
+            return gbs, f"device attributes: {pr.memory_clock_rate / 1e3:.0f} MHz x {pr.memory_bus_width}-bit x 2"
+    except Exception:
+        pass
+    return NOMINAL_HBM_GBS, "nominal: 3996 MHz x 8192-bit x 2"
+
+
 def source_hash():
     h = hashlib.sha256()
     for rel in PASS_KERNEL_SOURCES:
@@ -174,7 +191,25 @@ def cpu_baseline(n_total, seconds=10.0):
     med = statistics.median(times)
     return {"value": sample_n / med, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"first {sample_n} keys of the workload (same generator and seed), serial LSD radix sort, "
-                      f"median of {len(times)} runs"}
+                      f"median of {len(times)} runs",
+            "library_sort": library_sort_baseline(keys)}
+
+
+def library_sort_baseline(keys, seconds=5.0):
+    """Side baseline: the host's library comparison sort (numpy.sort, default kind) on one
+    core, on the same sample as the oracle."""
+    import numpy as np
+    times = []
+    t_end = time.perf_counter() + seconds
+    while True:
+        t0 = time.perf_counter()
+        np.sort(keys)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() > t_end or len(times) >= 20:
+            break
+    med = statistics.median(times)
+    return {"value": keys.size / med, "unit": UNIT, "cores": 1, "kind": "numpy.sort (library sort, one thread)",
+            "sample": f"the same {keys.size} keys, median of {len(times)} runs"}
 
 
 def run_reference(args):
@@ -284,6 +319,7 @@ def run_gbsort(args):
         return
 
     peak, peak_kind = peaks()
+    theo, theo_src = theoretical_hbm_gbs()
     # dominant kernel: the one-sweep digit pass (kernels 1..4 of each call)
     pass_ms = per_kernel[:, 1:5].mean()
     hist_ms = per_kernel[:, 0].mean()
@@ -303,9 +339,12 @@ def run_gbsort(args):
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": f"onesweep_pass_kernel<u32,keys,tile={gbsort.gbs_debug_radix_tile_keys(4)}>",
                      "peak_kind": f"{peak_kind} hbm_gbs",
+                     "theoretical_peak": theo, "theoretical_source": theo_src,
+                     "frac_of_theoretical": achieved / theo,
                      "algorithmic_bytes_per_launch": alg_pass, "avg_launch_ms": pass_ms},
         "whole_sort": {"achieved_gbs": alg_total / (ms_per_step / 1e3) / 1e9,
                        "frac_of_peak": alg_total / (ms_per_step / 1e3) / 1e9 / peak,
+                       "frac_of_theoretical": alg_total / (ms_per_step / 1e3) / 1e9 / theo,
                        "algorithmic_bytes": alg_total, "histogram_ms": hist_ms, "pass_ms": pass_ms,
                        "kernel_ms": per_kernel.mean(axis=0).tolist()},
         "cpu_baseline": cpu,
@@ -506,12 +545,15 @@ def run_secondary(args):
     else:
         dom_ms = float(per_kernel[dom_idx].sum() if extra.pop("sum_dominant", False) else per_kernel[dom_idx].mean())
     peak, peak_kind = peaks()
+    theo, _ = theoretical_hbm_gbs()
     line = {"workload": args.workload, "description": desc, "n": n, "ms_per_call": ms,
             "keys_per_s": n / (ms / 1e3), "algorithmic_bytes": alg_bytes,
             "achieved_gbs": alg_bytes / (ms / 1e3) / 1e9, "frac_of_peak": alg_bytes / (ms / 1e3) / 1e9 / peak,
             "dominant_kernel_ms": dom_ms, "dominant_kernel_gbs": dom_bytes / (dom_ms / 1e3) / 1e9,
             "dominant_kernel_frac": dom_bytes / (dom_ms / 1e3) / 1e9 / peak, "peak_gbs": peak,
-            "peak_kind": f"{peak_kind} hbm_gbs", "kernel_ms": per_kernel.tolist(), "launches": launches}
+            "peak_kind": f"{peak_kind} hbm_gbs", "theoretical_peak_gbs": theo,
+            "frac_of_theoretical": alg_bytes / (ms / 1e3) / 1e9 / theo,
+            "kernel_ms": per_kernel.tolist(), "launches": launches}
     if "comparators_per_call" in extra:
         line["comparators_per_s"] = extra["comparators_per_call"] / (ms / 1e3)
     line.update({k: v for k, v in extra.items() if k != "comparators_per_call"})

@@ -23,9 +23,11 @@ constexpr uint32_t FULL = 0xFFFFFFFFu;
 
 // ---------------------------------------------------------------------------
 // Block-wide exclusive scan of one value per thread for threads 0..255; all
-// threads of the block must call it.  wsum: 8 words of shared memory.
+// threads of the block must call it.  wsum: 8 words of shared memory.  TRAIL:
+// end with a barrier, so that wsum may be written again right after; a caller
+// that reaches a barrier of its own before touching wsum passes false.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t excl_scan_256(uint32_t v, uint32_t *wsum) {
+template <bool TRAIL = true> __device__ __forceinline__ uint32_t excl_scan_256(uint32_t v, uint32_t *wsum) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t x = v;
     if (tid < 256) {
@@ -41,7 +43,7 @@ __device__ __forceinline__ uint32_t excl_scan_256(uint32_t v, uint32_t *wsum) {
     if (tid < 256) {
         for (int w = 0; w < warp; ++w) base += wsum[w];
     }
-    __syncthreads();  // wsum may be reused right after
+    if (TRAIL) __syncthreads();
     return base + x - v;
 }
 
@@ -417,15 +419,18 @@ __device__ __forceinline__ void rank_warp(const K *tile_keys, uint32_t *whist, c
         // then matches no lane)
         uint32_t leader;
         asm("bfind.u32 %0, %1;" : "=r"(leader) : "r"(peers));
+        // peers below this lane; at the leader (the top lane) that is the
+        // group size minus one
+        const uint32_t below = __popc(peers & lt);
         // the leader's atomic, predicated rather than branched around
         uint32_t before = 0;
         asm volatile(
             "{\n\t.reg .pred p;\n\tsetp.eq.u32 p, %1, %2;\n\t@p atom.shared.add.u32 %0, [%3], %4;\n\t}"
             : "+r"(before)
-            : "r"((uint32_t)lane), "r"(leader), "r"(smem_u32(&whist[d])), "r"((uint32_t)__popc(peers))
+            : "r"((uint32_t)lane), "r"(leader), "r"(smem_u32(&whist[d])), "r"(below + 1u)
             : "memory");
         const uint32_t b = __shfl_sync(FULL, before, (int)leader);
-        ranks.set(i, ok ? b + __popc(peers & lt) : 0u);
+        ranks.set(i, ok ? b + below : 0u);
     }
 }
 
@@ -741,7 +746,8 @@ __global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
         cnt = tile_digit_count<WARPS>(sm.whist, tid);
         if (!faulty) st_relaxed_gpu(my_status + tid, ((tile == 0 ? st_inc : st_agg) << STATUS_COUNT_BITS) | cnt);
     }
-    const uint32_t local = excl_scan_256(cnt, sm.wsum);
+    // (wsum is not written again before the barrier after the offsets)
+    const uint32_t local = excl_scan_256<false>(cnt, sm.wsum);
     if (tid < 256) {
         // sorted-tile slot of each warp's first key of digit tid
 #pragma unroll 4
