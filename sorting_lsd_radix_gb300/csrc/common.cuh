@@ -204,6 +204,12 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, u
         : "memory");
 }
 
+// Hint: fetch global bytes [src, src + bytes) into L2 (no completion signal,
+// nothing written).  src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Records the first device-side error in the header.
 __device__ __forceinline__ void record_error(Header *h, uint32_t code, uint32_t detail) {
     if (atomicCAS(&h->error, 0u, code) == 0u) atomicExch(&h->error_detail, detail);

@@ -298,6 +298,10 @@ struct PassParams {
     uint32_t spin_limit;
     int fault_pass;
     uint32_t fault_tile;
+    // the CTA of tile t prefetches tile t + prefetch_ahead into L2 (0: none);
+    // set to about half the CTAs resident on the device, so the data arrive
+    // well before that tile's CTA starts and are still in L2 when it does
+    uint32_t prefetch_ahead;
 };
 
 template <typename K> struct Xform;
@@ -684,6 +688,11 @@ __global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
             bulk_g2s(sm.keys, ksrc + (size_t)spec * TILE, TILE * (uint32_t)sizeof(K), &sm.bar);
             if (PAIRS) bulk_g2s(sm.vals, vsrc + (size_t)spec * TILE, TILE * (uint32_t)VB, &sm.bar);
         }
+        const size_t pf = (size_t)spec + prm.prefetch_ahead;
+        if (prm.prefetch_ahead != 0 && aligned && (pf + 1) * TILE <= (size_t)prm.n) {
+            prefetch_l2_bulk(ksrc + pf * TILE, TILE * (uint32_t)sizeof(K));
+            if (PAIRS) prefetch_l2_bulk(vsrc + pf * TILE, TILE * (uint32_t)VB);
+        }
         sm.tile = atomicAdd(&hdr->tile_counter[prm.pass], 1u);
     }
     const uint32_t dbase = (tid < 256) ? prm.digit_base[prm.pass * 256 + tid] : 0u;
@@ -956,6 +965,7 @@ cudaError_t launch_passes(const RadixJob &job, cudaStream_t stream, int *launche
     prm.fault_pass = job.fault_pass;
     prm.fault_tile = job.fault_tile;
     prm.digit_base = job.digit_base;
+    prm.prefetch_ahead = (uint32_t)(device_sms() * (GBS_PASS_THREADS_PER_SM / THREADS) / 2);
     for (int p = 0; p < job.num_passes; ++p) {
         prm.pass = p;
         prm.shift = job.begin_bit + 8 * p;
