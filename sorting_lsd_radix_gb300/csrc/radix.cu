@@ -192,15 +192,30 @@ __global__ void __launch_bounds__(HIST_THREADS, 1) upfront_histogram_kernel(cons
     const uint4 *vec = reinterpret_cast<const uint4 *>(prm.keys);
     const size_t stride = (size_t)gridDim.x * HIST_THREADS;
     size_t i = (size_t)blockIdx.x * HIST_THREADS + tid;
-    for (; i + (HIST_UNROLL - 1) * stride < nvec; i += HIST_UNROLL * stride) {
+    // software-pipelined: the next HIST_UNROLL vectors are in flight while
+    // the current ones are counted
+    if (i + (HIST_UNROLL - 1) * stride < nvec) {
         uint4 r[HIST_UNROLL];
 #pragma unroll
         for (int u = 0; u < HIST_UNROLL; ++u) r[u] = __ldcs(vec + i + u * stride);
+        for (;;) {
+            const size_t inext = i + HIST_UNROLL * stride;
+            const bool more = inext + (HIST_UNROLL - 1) * stride < nvec;
+            uint4 q[HIST_UNROLL];
+            if (more) {
 #pragma unroll
-        for (int u = 0; u < HIST_UNROLL; ++u) {
-            const K *ks = reinterpret_cast<const K *>(&r[u]);
+                for (int u = 0; u < HIST_UNROLL; ++u) q[u] = __ldcs(vec + inext + u * stride);
+            }
 #pragma unroll
-            for (int e = 0; e < C::PER_VEC; ++e) count(ks[e]);
+            for (int u = 0; u < HIST_UNROLL; ++u) {
+                const K *ks = reinterpret_cast<const K *>(&r[u]);
+#pragma unroll
+                for (int e = 0; e < C::PER_VEC; ++e) count(ks[e]);
+            }
+            i = inext;
+            if (!more) break;
+#pragma unroll
+            for (int u = 0; u < HIST_UNROLL; ++u) r[u] = q[u];
         }
     }
     for (; i < nvec; i += stride) {
