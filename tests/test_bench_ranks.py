@@ -84,3 +84,28 @@ def test_reference_arm_line_on_rank_zero():
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "keys/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_pin_rate_peak_and_library_sort_side_baseline():
+    import numpy as np
+    b = _bench()
+    gbs, source = b.theoretical_hbm_gbs()
+    if source.startswith("nominal"):
+        # 3996 MHz, double data rate, 8192-bit bus: 8183.8 GB/s
+        assert gbs == pytest.approx(2 * 3996e6 * 8192 / 8 / 1e9)
+    else:
+        assert 1000.0 < gbs < 20000.0
+    keys = np.arange(1 << 16, dtype=np.uint32)[::-1].copy()
+    side = b.library_sort_baseline(keys, seconds=0.05)
+    assert side["unit"] == "keys/s" and side["value"] > 0 and side["cores"] == 1
+
+
+def test_recorded_traffic_tracks_the_pass_kernel_source():
+    """The committed ncu summary carries a hash of the pass kernel's sources; the bench reports its
+    DRAM traffic (scaled from 2^26 keys) only while that hash matches."""
+    b = _bench()
+    rec = b.recorded_traffic(1 << 26)
+    if rec is None:
+        pytest.skip("pass kernel changed since its ncu capture (traffic reported as null)")
+    # one read and one write of 4-byte keys, less what is still in L2 at kernel end
+    assert 0.85 * 8 * (1 << 26) < rec <= 1.05 * 8 * (1 << 26)
