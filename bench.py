@@ -243,19 +243,29 @@ def run_gbsort(args):
     dist = None
     if world > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl")
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     from sorting_lsd_radix_gb300 import build as gbuild
     gbuild.build()
-    from sorting_lsd_radix_gb300 import gbsort
+    from sorting_lsd_radix_gb300 import gbsort, sharded
 
     n = args.n
     host = wl.uniform_u32(n, SEED + rank)
     d_in = torch.from_numpy(host).cuda()
-    d_out = torch.empty_like(d_in)
-    _, temp = gbsort.gbs_sort_keys(d_in, d_out, return_temp=True)
-    torch.cuda.synchronize()
-    launches = gbsort.gbs_debug_last_launch_count()
     stream = torch.cuda.current_stream()
+    if world == 1:
+        d_out = torch.empty_like(d_in)
+        _, temp = gbsort.gbs_sort_keys(d_in, d_out, return_temp=True)
+
+        def step():
+            gbsort.gbs_sort_keys(d_in, d_out, temp=temp)
+            return d_out
+    else:
+        # one array of world * n keys held in shards: the sample-sort exchange across the GPUs
+        def step():
+            return sharded.sharded_sort(d_in)[0]
+    out = step()
+    torch.cuda.synchronize()
+    launches = gbsort.gbs_debug_last_launch_count()  # kernels of the step's last sorting call
 
     def barrier():
         if dist is not None:
@@ -264,8 +274,8 @@ def run_gbsort(args):
 
     # ---- device-resident timing: K steps between two events ----------------
     for _ in range(args.warmup):
-        gbsort.gbs_sort_keys(d_in, d_out, temp=temp)
-    # per-kernel events for every timed step (histogram, 4 passes)
+        out = step()
+    # per-kernel events of every timed step's (last) sorting call: histogram and 4 passes
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(launches + 1)] for _ in range(args.steps)]
     for evs in events:  # torch creates the CUDA event on first record
         for e in evs:
@@ -276,23 +286,58 @@ def run_gbsort(args):
     start.record(stream)
     for s in range(args.steps):
         gbsort.gbs_debug_set_timing_events(events[s])
-        gbsort.gbs_sort_keys(d_in, d_out, temp=temp)
+        out = step()
     stop.record(stream)
     gbsort.gbs_debug_set_timing_events(None)
     barrier()
     clocks = sampler.stop()
     ms = max_over_ranks(start.elapsed_time(stop), dist, "cuda")
     ms_per_step = ms / args.steps
-    status = gbsort.gbs_get_status(temp)
+    status = gbsort.gbs_get_status(temp) if world == 1 else gbsort.GBS_OK
     per_kernel = np.array([[ev[i].elapsed_time(ev[i + 1]) for i in range(launches)] for ev in events])
 
-    # correctness spot check of the timed output (full check is in the tests)
-    out_host = d_out.cpu().numpy()
+    # correctness spot check of the timed output (full checks are in the tests): sorted, and for
+    # the sharded sort every rank's last key is at most the next rank's first key
+    out_host = out.cpu().numpy()
     ok = bool((out_host[1:] >= out_host[:-1]).all()) and status == gbsort.GBS_OK
+    if dist is not None:
+        edge = torch.tensor([int(out_host[0]) if out_host.size else 2**32, int(out_host[-1]) if out_host.size else -1],
+                            dtype=torch.int64, device="cuda")
+        edges = [torch.empty_like(edge) for _ in range(world)]
+        dist.all_gather(edges, edge)
+        e = [t.cpu().tolist() for t in edges]
+        ok = ok and all(e[r][1] <= e[r + 1][0] for r in range(world - 1) if e[r][1] >= 0 and e[r + 1][0] < 2**32)
+        total = torch.tensor([out_host.size], dtype=torch.int64, device="cuda")
+        dist.all_reduce(total)
+        ok = ok and int(total.item()) == world * n
 
     # ---- end to end: the C-ABI host-buffer entry point (copy in, sort, copy out)
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and world > 1:
+        # the sharded sort from host memory: each rank copies its shard in, the GPUs sort the whole
+        # array together, each rank copies its part of the result back
+        h_in = torch.from_numpy(host).pin_memory()
+
+        def e2e_step():
+            part = sharded.sharded_sort(h_in.cuda(non_blocking=True))[0]
+            return part.cpu()
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        k = max(3, min(args.steps, 10))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k):
+            hv = e2e_step()
+        e1.record(stream)
+        barrier()
+        ems = max_over_ranks(e0.elapsed_time(e1) / k, dist, "cuda")
+        hvn = hv.numpy()
+        ok = ok and bool((hvn[1:] >= hvn[:-1]).all())
+        e2e = {"value": job_throughput(world, n, ems), "unit": UNIT, "h2d_bytes_per_step": 4 * n,
+               "d2h_bytes_per_step": 4 * int(hvn.size), "ms_per_step": ems,
+               "api": "sorting_lsd_radix_gb300.sharded.sharded_sort on a copy of the host shard"}
+    elif not args.no_e2e:
         h_in = torch.from_numpy(host).pin_memory()
         h_out = torch.empty_like(h_in).pin_memory()
         _, htemp = gbsort.gbs_sort_keys_host(h_in, h_out, temp=None, return_temp=True)
@@ -364,7 +409,9 @@ def run_gbsort(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic",
         "config": {"workload": WORKLOAD, "n": n, "key_type": "u32", "begin_bit": 0, "end_bit": 32,
                    "seed": SEED, "l2": "input 400 MB > L2; no flush between steps",
-                   "parallelism": f"{world} independent sorts (one per GPU)"},
+                   "parallelism": (f"one array of {world} x {n} keys sharded over {world} GPUs: digit histograms, "
+                                   f"one partition pass, one all-to-all-v exchange (NCCL), local radix sort"
+                                   if world > 1 else "one GPU")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": f"onesweep_pass_kernel<u32,keys,tile={gbsort.gbs_debug_radix_tile_keys(4)}>",
@@ -379,7 +426,7 @@ def run_gbsort(args):
                        "kernel_ms": per_kernel.mean(axis=0).tolist()},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": launches * args.steps,
+        "gpu_launches": (launches if world == 1 else launches + 3) * args.steps,
         "clocks": clocks,
         "check": {"sorted": ok, "status": gbsort.status_string(status)},
     }

@@ -72,7 +72,8 @@ typedef enum {
 /* Largest number of keys a radix sort call accepts: per-digit counts are
  * kept in 29-bit fields of the tile status words. */
 #define GBS_MAX_RADIX_KEYS ((size_t)((1u << 29) - 1))
-/* Longest segment of gbs_segmented_sort (one CTA sorts one segment on chip). */
+/* Longest segment that one CTA's bitonic network sorts on chip; longer
+ * segments take the radix path. */
 #define GBS_MAX_SEGMENT_LEN ((size_t)16384)
 
 /*
@@ -139,11 +140,18 @@ gbs_status gbs_sort_pairs64(void *d_temp, size_t *temp_bytes, gbs_key_type key_t
 
 /*
  * gbs_segmented_sort — sort each of num_segments consecutive segments of
- * segment_len keys independently, over the full key width, with the bitonic
- * network ("并行排序" §3.3-3.5, §4.2-4.3).  A segment whose length is not a
- * power of two is padded on chip with a sentinel that sorts after every key.
- *   segment_len  1 .. GBS_MAX_SEGMENT_LEN (0 segments or length 0: no work)
+ * segment_len keys independently, over the full key width.  Segments of up
+ * to GBS_MAX_SEGMENT_LEN keys run the bitonic network, one segment per CTA
+ * (or warp), padded on chip with a sentinel that sorts after every key when
+ * the length is not a power of two ("并行排序" §3.3-3.5, §4.2-4.3).  Longer
+ * segments run the radix sort, one segment after another in one radix work
+ * area (the bitonic network of one CTA holds at most 2^14 keys).
+ *   segment_len  1 .. GBS_MAX_RADIX_KEYS (0 segments or length 0: no work)
  *   d_keys_out may equal d_keys_in.
+ *   d_temp       work buffer: a status header, plus a radix work area for
+ *                segment_len keys when segment_len > GBS_MAX_SEGMENT_LEN
+ * Device-side timeouts of the radix part are reported by gbs_get_status on
+ * d_temp (the first one wins).
  */
 gbs_status gbs_segmented_sort(void *d_temp, size_t *temp_bytes, gbs_key_type key_type,
                               const void *d_keys_in, void *d_keys_out,
@@ -200,18 +208,29 @@ gbs_status gbs_digit_histograms(void *d_temp, size_t *temp_bytes, gbs_key_type k
  * allocating call is made.
  *   n  at most GBS_NOALLOC_MAX_KEYS; larger n returns GBS_ERR_UNSUPPORTED
  *      and launches nothing.
- * The first call on each device looks up the array's device address (a
- * cudaGetSymbolAddress with that device current); make that first call
- * before any stream capture.  Every call, on every stream, shares the one
- * array: calls whose work overlaps on the GPU race and corrupt each other's
- * results, so serialise them (one stream, or events).  The array keeps the
- * last call's contents; each call clears what it needs to start at zero.
- * Device-side timeouts are recorded in the array's header and are not
- * reported by gbs_get_status.
+ * Every call asks the runtime for the array's device address on the current
+ * device (cudaGetSymbolAddress); the first call on a device also loads the
+ * library's device code there, so make that first call before any stream
+ * capture.  Every call, on every stream, shares the one array: calls whose
+ * work overlaps on the GPU race and corrupt each other's results, so
+ * serialise them (one stream, or events).  The array keeps the last call's
+ * contents; each call clears what it needs to start at zero.  A device-side
+ * timeout is recorded in the array's header; gbs_get_status_noalloc reports
+ * it.
  */
 #define GBS_NOALLOC_MAX_KEYS ((size_t)1 << 20)
 gbs_status gbs_sort_keys_noalloc(gbs_key_type key_type, const void *d_keys_in, void *d_keys_out, size_t n,
                                  int begin_bit, int end_bit, int descending, void *stream);
+
+/*
+ * gbs_get_status_noalloc — gbs_get_status for gbs_sort_keys_noalloc, whose
+ * work buffer is the library's own array on the current device: synchronises
+ * `stream`, then returns GBS_ERR_TIMEOUT if the last call on this device
+ * recorded a device-side timeout, else GBS_OK (GBS_ERR_CUDA if the stream or
+ * the read reports an error).  Allocates nothing.  The web pages have no
+ * counterpart.
+ */
+gbs_status gbs_get_status_noalloc(void *stream);
 
 /*
  * gbs_get_status — synchronises `stream`, then reports GBS_ERR_TIMEOUT if the

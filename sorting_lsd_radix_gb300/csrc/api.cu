@@ -160,6 +160,12 @@ gbs_status radix_common(void *d_temp, size_t *temp_bytes, gbs_key_type kt, const
 }  // namespace
 
 namespace gbs {
+void debug_fault_settings(int *fault_pass, uint32_t *fault_tile, uint32_t *spin_limit) {
+    *fault_pass = g_fault_pass;
+    *fault_tile = g_fault_tile;
+    *spin_limit = g_spin_limit;
+}
+
 void timing_mark(cudaStream_t s) {
     if (t_events && t_event_next > 0 && t_event_next < t_event_count &&
         cudaEventRecord(reinterpret_cast<cudaEvent_t>(t_events[t_event_next++]), s) != cudaSuccess)
@@ -228,11 +234,20 @@ gbs_status gbs_segmented_sort(void *d_temp, size_t *temp_bytes, gbs_key_type key
     t_launches = 0;
     const int kb = key_bytes_of(key_type);
     if (kb == 0 || temp_bytes == nullptr) return GBS_ERR_INVALID_ARG;
-    if (segment_len > GBS_MAX_SEGMENT_LEN) return GBS_ERR_UNSUPPORTED;
+    if (segment_len > GBS_MAX_RADIX_KEYS) return GBS_ERR_UNSUPPORTED;
     if (num_segments != 0 && segment_len != 0 && num_segments > (size_t)-1 / segment_len / 8)
         return GBS_ERR_INVALID_ARG;
+    // segments longer than one CTA's network: the radix sort, one segment after another in a
+    // shared radix work area (as gbs_segmented_sort_offsets does for its long segments)
+    const bool radix = segment_len > GBS_MAX_SEGMENT_LEN;
+    size_t need = sizeof(Header);
+    if (radix) {
+        gbs_status st = radix_common(nullptr, &need, key_type, nullptr, nullptr, nullptr, nullptr, 0, segment_len, 0,
+                                     8 * kb, descending, stream);
+        if (st != GBS_OK) return st;
+    }
     bool query = false;
-    gbs_status st = check_temp(d_temp, temp_bytes, sizeof(Header), &query);
+    gbs_status st = check_temp(d_temp, temp_bytes, need, &query);
     if (st != GBS_OK || query) return st;
     const size_t total = num_segments * segment_len;
     if (total > 0 && (d_keys_in == nullptr || d_keys_out == nullptr)) return GBS_ERR_INVALID_ARG;
@@ -241,6 +256,17 @@ gbs_status gbs_segmented_sort(void *d_temp, size_t *temp_bytes, gbs_key_type key
     if (e != cudaSuccess) return GBS_ERR_CUDA;
     if (total == 0) return GBS_OK;
     if (segment_len == 1) return from_cuda(copy_if_needed(d_keys_in, d_keys_out, total * kb, s));
+    if (radix) {  // the launch count accumulates over the segments' sorts
+        for (size_t i = 0; i < num_segments; ++i) {
+            const size_t lo = i * segment_len * kb;
+            size_t have = need;
+            st = radix_common(d_temp, &have, key_type, static_cast<const unsigned char *>(d_keys_in) + lo,
+                              static_cast<unsigned char *>(d_keys_out) + lo, nullptr, nullptr, 0, segment_len, 0,
+                              8 * kb, descending, stream, /*keep_error=*/true);
+            if (st != GBS_OK) return st;
+        }
+        return GBS_OK;
+    }
     timing_start(s);
     return from_cuda(gbs::launch_segmented_bitonic((int)key_type, kb, d_keys_in, d_keys_out, num_segments,
                                                    segment_len, descending != 0, s, &t_launches));

@@ -147,9 +147,16 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 // Ballot of "(x & m) != 0" over a fully active warp, as one and/setp/vote
 // sequence.  Measured on sm_103a, __ballot_sync on the same comparison issues
 // about 3.7 integer-pipe instructions per ballot and this form about 1.4.
+#ifndef GBS_BALLOT_VOLATILE
+#define GBS_BALLOT_VOLATILE 1
+#endif
 __device__ __forceinline__ uint32_t ballot_bits(uint32_t x, uint32_t m) {
     uint32_t r;
+#if GBS_BALLOT_VOLATILE
     asm volatile(
+#else
+    asm(
+#endif
         "{\n\t.reg .pred p;\n\t.reg .b32 t;\n\tand.b32 t, %1, %2;\n\tsetp.ne.u32 p, t, 0;\n\t"
         "vote.sync.ballot.b32 %0, p, 0xffffffff;\n\t}"
         : "=r"(r)

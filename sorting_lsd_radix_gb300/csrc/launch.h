@@ -56,6 +56,10 @@ struct RadixJob {
     uint32_t fault_tile;
 };
 
+// The test hooks' look-back fault and bounded-wait limit (see
+// gbs_debug_set_lookback_fault); the defaults when the hook is off.
+void debug_fault_settings(int *fault_pass, uint32_t *fault_tile, uint32_t *spin_limit);
+
 // Kernel timing hook (see gbs_debug_set_timing_events): records the next
 // caller-provided event on the stream after a launch, if the hook is set.
 void timing_mark(cudaStream_t stream);

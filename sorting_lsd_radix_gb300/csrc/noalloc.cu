@@ -9,8 +9,6 @@
 // pool is fixed up front.  Such callers still own their keys; only the
 // scratch space (header, histograms, look-back status words and the
 // alternate key buffer) comes from here.
-#include <mutex>
-
 #include "../../include/gbsort.h"
 #include "launch.h"
 
@@ -33,22 +31,18 @@ constexpr size_t kScratchBytes = kHeader + 2 * kHist + kStatus + kKeys;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-// Device address of g_noalloc_scratch, looked up once per device.  In host
-// code the array's name is only a host-side stand-in, never a device address.
-constexpr int kMaxDevices = 64;
-void *g_scratch_addr[kMaxDevices] = {};
-std::mutex g_scratch_mutex;
-
+// Device address of g_noalloc_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, never a device address, so
+// every call asks the runtime for the address on the device that is current
+// now.  The first call on a device also loads the library's device code there
+// (the array is created with it); later calls are a table lookup.  Asking
+// each time, instead of caching the pointer, keeps the address right after a
+// cudaDeviceReset, which destroys the array and makes a new one at the next
+// call.
 gbs_status scratch_for_current_device(unsigned char **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GBS_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return GBS_ERR_CUDA;
-        g_scratch_addr[dev] = p;
-    }
-    *out = reinterpret_cast<unsigned char *>(g_scratch_addr[dev]);
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return GBS_ERR_CUDA;
+    *out = reinterpret_cast<unsigned char *>(p);
     return GBS_OK;
 }
 
@@ -109,9 +103,17 @@ extern "C" gbs_status gbs_sort_keys_noalloc(gbs_key_type key_type, const void *d
     job.digit_base = reinterpret_cast<uint32_t *>(scratch + off_base);
     job.status = reinterpret_cast<uint32_t *>(scratch + off_status);
     job.num_tiles = tiles;
-    job.spin_limit = 1u << 22;
-    job.fault_pass = -1;
-    job.fault_tile = 0;
+    gbs::debug_fault_settings(&job.fault_pass, &job.fault_tile, &job.spin_limit);
     int launches = 0;
     return gbs::launch_radix_sort(job, s, &launches) == cudaSuccess ? GBS_OK : GBS_ERR_CUDA;
+}
+
+extern "C" gbs_status gbs_get_status_noalloc(void *stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return GBS_ERR_CUDA;
+    unsigned char *scratch = nullptr;
+    const gbs_status st = scratch_for_current_device(&scratch);
+    if (st != GBS_OK) return st;
+    uint32_t err = 0;  // first word of the header: the first device-side error of the last call
+    if (cudaMemcpy(&err, scratch, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess) return GBS_ERR_CUDA;
+    return err ? GBS_ERR_TIMEOUT : GBS_OK;
 }

@@ -66,6 +66,12 @@ template <bool TRAIL = true> __device__ __forceinline__ uint32_t excl_scan_256(u
 #ifndef GBS_PEER_IMAD
 #define GBS_PEER_IMAD 0
 #endif
+#ifndef GBS_ATOM_CLOBBER
+#define GBS_ATOM_CLOBBER 1
+#endif
+#ifndef GBS_STORE_FULL
+#define GBS_STORE_FULL 0
+#endif
 
 struct PeerTableLane {
     uint32_t c[5];  // 0 where bit k of the lane index is set, all ones where it is clear
@@ -287,6 +293,8 @@ template <typename K, int VB, int THREADS, int ITEMS> struct PassSmem {
     uint32_t binoff[256];  // global position of sorted-tile slot 0 of each digit
     uint32_t wsum[8];
     uint32_t tile;
+    uint32_t num_active;  // active passes of this call
+    uint32_t ordinal;     // rank of this pass among them
     alignas(8) uint64_t bar;
 };
 
@@ -443,11 +451,22 @@ __device__ __forceinline__ void rank_warp(const K *tile_keys, uint32_t *whist, c
         const uint32_t below = __popc(peers & lt);
         // the leader's atomic, predicated rather than branched around
         uint32_t before = 0;
+#if GBS_ATOM_CLOBBER
         asm volatile(
             "{\n\t.reg .pred p;\n\tsetp.eq.u32 p, %1, %2;\n\t@p atom.shared.add.u32 %0, [%3], %4;\n\t}"
             : "+r"(before)
             : "r"((uint32_t)lane), "r"(leader), "r"(smem_u32(&whist[d])), "r"(below + 1u)
             : "memory");
+#else
+        // volatile keeps the warp's atomics in program order; no memory
+        // clobber: nothing reads the counters through ordinary loads before
+        // the CTA barrier that ends the rank, so the compiler may move other
+        // items' work across the atomic
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.eq.u32 p, %1, %2;\n\t@p atom.shared.add.u32 %0, [%3], %4;\n\t}"
+            : "+r"(before)
+            : "r"((uint32_t)lane), "r"(leader), "r"(smem_u32(&whist[d])), "r"(below + 1u));
+#endif
         const uint32_t b = __shfl_sync(FULL, before, (int)leader);
         ranks.set(i, ok ? b + below : 0u);
     }
@@ -473,6 +492,21 @@ __device__ __forceinline__ void store_tile(const K *sk, const ValueT<VB> *sv, co
             kdst[pos] = DEC ? Xform<K>::dec(key, prm) : key;
             if (VB) vdst[pos] = sv[j];
         }
+    }
+}
+
+// Full-tile form: every slot holds a key, and the caller has checked once for
+// the whole tile that every digit's positions lie inside the output.
+template <bool DEC, bool BYTE, typename K, int VB, int THREADS, int ITEMS>
+__device__ __forceinline__ void store_tile_full(const K *sk, const ValueT<VB> *sv, const uint32_t *binoff, K *kdst,
+                                                ValueT<VB> *vdst, const PassParams &prm, int tid) {
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const uint32_t j = (uint32_t)(tid + it * THREADS);
+        const K key = sk[j];
+        const uint32_t pos = binoff[pass_digit<BYTE>(key, prm)] + j;
+        kdst[pos] = DEC ? Xform<K>::dec(key, prm) : key;
+        if (VB) vdst[pos] = sv[j];
     }
 }
 
@@ -595,6 +629,120 @@ template <typename K, int VB> struct PassIO {
     }
 };
 
+// Everything after the tile load: stable rank, tile counts and aggregate,
+// reorder in shared memory, look-back, scatter.  FULLTILE: the tile holds
+// TILE keys (every tile but a ragged last one).
+template <bool FULLTILE, typename K, int VB, int THREADS, int ITEMS, bool BYTE>
+__device__ __forceinline__ void pass_tile(PassSmem<K, VB, THREADS, ITEMS> &sm, const PassParams &prm, Header *hdr,
+                                          const uint32_t valid, const bool first) {
+    constexpr bool PAIRS = VB != 0;
+    using V = ValueT<VB>;
+    constexpr int WARPS = THREADS / 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // ---- stable rank within the tile --------------------------------------
+    K keys[ITEMS];
+    PackedRanks<ITEMS> ranks;
+    uint32_t *whist = sm.whist[warp];
+    if (first)
+        rank_warp<true, BYTE, FULLTILE>(sm.keys, whist, prm, warp, lane, valid, keys, ranks);
+    else
+        rank_warp<false, BYTE, FULLTILE>(sm.keys, whist, prm, warp, lane, valid, keys, ranks);
+    __syncthreads();
+
+    // values not needed during the rank are fetched now, so that they hold no
+    // registers across it
+    const uint32_t tile = sm.tile, A = sm.num_active, k = sm.ordinal;
+    const bool last = (k + 1 == A) && !prm.identity;
+    // chained-scan states of this pass (rotated by ordinal, see common.cuh)
+    const uint32_t st_agg = 1u + 2u * (k % 3u), st_inc = 2u + 2u * (k % 3u);
+    const uint32_t dbase = (tid < 256) ? prm.digit_base[prm.pass * 256 + tid] : 0u;
+    const PassIO<K, VB> io(prm, A, k);
+    K *kdst = io.kdst;
+    V *vdst = io.vdst;
+
+    // ---- tile digit counts, warp offsets, publish the aggregate ------------
+    uint32_t cnt = 0;
+    uint32_t *my_status = prm.status + (size_t)tile * 256;
+    const bool faulty = (prm.fault_pass == prm.pass) && (prm.fault_tile == tile);
+    if (tid < 256) {
+        cnt = tile_digit_count<WARPS>(sm.whist, tid);
+        if (!faulty) st_relaxed_gpu(my_status + tid, ((tile == 0 ? st_inc : st_agg) << STATUS_COUNT_BITS) | cnt);
+    }
+    // (wsum is not written again before the barrier after the offsets)
+    const uint32_t local = excl_scan_256<false>(cnt, sm.wsum);
+    if (tid < 256) {
+        // sorted-tile slot of each warp's first key of digit tid
+#pragma unroll 4
+        for (int w = 0; w < WARPS; ++w) sm.whist[w][tid] += local;
+    }
+    __syncthreads();
+
+    // ---- reorder the tile in shared memory by (digit, rank) ---------------
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) {
+        const uint32_t idx = (uint32_t)warp * (ITEMS * 32) + i * 32 + lane;
+        if (FULLTILE || idx < valid) {
+            const uint32_t slot = ranks.get(i) + whist[pass_digit<BYTE>(keys[i], prm)];
+            if (PAIRS) ranks.replace(i, slot);
+            sm.keys[slot] = keys[i];
+        }
+    }
+    if (PAIRS) {
+        V vals[ITEMS];
+#pragma unroll
+        for (int i = 0; i < ITEMS; ++i) {
+            const uint32_t idx = (uint32_t)warp * (ITEMS * 32) + i * 32 + lane;
+            vals[i] = (idx < valid) ? sm.vals[idx] : V(0);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < ITEMS; ++i) {
+            const uint32_t idx = (uint32_t)warp * (ITEMS * 32) + i * 32 + lane;
+            if (idx < valid) sm.vals[ranks.get(i)] = vals[i];
+        }
+    }
+
+    // ---- decoupled look-back over the predecessors' status words ----------
+    // Each digit's thread reads LOOKBACK_WINDOW predecessors per round trip
+    // (registers are free again: the tile's keys now sit in shared memory),
+    // adds the aggregates from the nearest one back to the first inclusive
+    // prefix, and waits (bounded) only at a predecessor that has published
+    // nothing yet.
+    bool out_of_range = false;
+    if (tid < 256) {
+        uint32_t excl = 0;
+        if (tile > 0) {
+            excl = lookback_excl(prm, hdr, tile, tid, st_agg, st_inc);
+            if (!faulty)
+                st_relaxed_gpu(my_status + tid, (st_inc << STATUS_COUNT_BITS) | ((excl + cnt) & STATUS_COUNT_MASK));
+        }
+        sm.binoff[tid] = dbase + excl - local;
+        // every position of digit tid lies in [dbase + excl, dbase + excl + cnt); with counts
+        // from a tile that never landed (a bounded wait gave up) they may not
+        out_of_range = cnt != 0 && (uint64_t)dbase + excl + cnt > (uint64_t)prm.n;
+    }
+#if GBS_STORE_FULL
+    if (FULLTILE) {
+        if (__syncthreads_or(out_of_range)) {
+            if (tid == 0) record_error(hdr, ERR_COPY_TIMEOUT, ((uint32_t)prm.pass << 24) | (tile & 0xFFFFFFu));
+            return;
+        }
+        if (last)
+            store_tile_full<true, BYTE, K, VB, THREADS, ITEMS>(sm.keys, sm.vals, sm.binoff, kdst, vdst, prm, tid);
+        else
+            store_tile_full<false, BYTE, K, VB, THREADS, ITEMS>(sm.keys, sm.vals, sm.binoff, kdst, vdst, prm, tid);
+        return;
+    }
+#endif
+    (void)out_of_range;
+    __syncthreads();
+
+    if (last)
+        store_tile<true, BYTE, K, VB, THREADS>(sm.keys, sm.vals, sm.binoff, valid, kdst, vdst, prm, tid);
+    else
+        store_tile<false, BYTE, K, VB, THREADS>(sm.keys, sm.vals, sm.binoff, valid, kdst, vdst, prm, tid);
+}
+
 // Launch shapes of the pass kernel (threads per CTA x keys per thread).  Every
 // shape keeps PASS_THREADS_PER_SM threads resident per SM (64 registers per
 // thread); smaller CTAs give more independent tiles per SM, whose latency-bound
@@ -653,7 +801,7 @@ __global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
     extern __shared__ __align__(128) unsigned char smem_raw[];
     S &sm = *reinterpret_cast<S *>(smem_raw);
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     Header *hdr = prm.hdr;
     const uint32_t A = hdr->num_active;
     const bool active = (hdr->active_mask >> prm.pass) & 1u;
@@ -674,157 +822,62 @@ __global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
     const uint32_t k = hdr->ordinal[prm.pass];
     // the key code is applied on the first active pass's load and undone on
     // the last one's store, unless it is the identity (unsigned ascending)
-    const bool first = (k == 0) && !prm.identity, last = (k + 1 == A) && !prm.identity;
+    const bool first = (k == 0) && !prm.identity;
 
     const PassIO<K, VB> io(prm, A, k);
     const K *ksrc = io.ksrc;
-    K *kdst = io.kdst;
     const V *vsrc = io.vsrc;
-    V *vdst = io.vdst;
 
-    // chained-scan states of this pass (rotated by ordinal, see common.cuh)
-    const uint32_t st_agg = 1u + 2u * (k % 3u), st_inc = 2u + 2u * (k % 3u);
     const bool aligned = ((reinterpret_cast<uintptr_t>(ksrc) & 15) == 0) &&
                          (!PAIRS || ((reinterpret_cast<uintptr_t>(vsrc) & 15) == 0));
     const uint32_t tx_bytes = TILE * (uint32_t)(sizeof(K) + VB);
 
     // ---- ticket and tile load ---------------------------------------------
-    // Tiles are taken in ticket order (forward progress of the look-back).
-    // The ticket usually equals blockIdx.x, so that tile's bulk copy is issued
-    // before the ticket atomic returns; a different ticket waits for the
-    // speculative copy to land and loads its own tile.
-    const uint32_t spec = blockIdx.x;
-    const bool spec_ok = aligned && ((size_t)(spec + 1) * TILE <= (size_t)prm.n);
+    // Tiles are taken in ticket order, which guarantees the look-back's
+    // forward progress whatever order the CTAs start in.  The ticket is taken
+    // first and then that tile is copied: the tickets reach L2 in an order
+    // that rarely matches the CTAs' launch order, so a copy issued before the
+    // ticket returns would almost always fetch the wrong tile.
     if (tid == 0) {
         mbar_init(&sm.bar, 1);
         fence_mbar_init();
-        if (spec_ok) {
+        const uint32_t t = atomicAdd(&hdr->tile_counter[prm.pass], 1u);
+        sm.tile = t;
+        const size_t start = (size_t)t * TILE;
+        if (aligned && start + TILE <= (size_t)prm.n) {
             mbar_arrive_expect_tx(&sm.bar, tx_bytes);
-            bulk_g2s(sm.keys, ksrc + (size_t)spec * TILE, TILE * (uint32_t)sizeof(K), &sm.bar);
-            if (PAIRS) bulk_g2s(sm.vals, vsrc + (size_t)spec * TILE, TILE * (uint32_t)VB, &sm.bar);
+            bulk_g2s(sm.keys, ksrc + start, TILE * (uint32_t)sizeof(K), &sm.bar);
+            if (PAIRS) bulk_g2s(sm.vals, vsrc + start, TILE * (uint32_t)VB, &sm.bar);
         }
-        const size_t pf = (size_t)spec + prm.prefetch_ahead;
+        const size_t pf = (size_t)t + prm.prefetch_ahead;
         if (prm.prefetch_ahead != 0 && aligned && (pf + 1) * TILE <= (size_t)prm.n) {
             prefetch_l2_bulk(ksrc + pf * TILE, TILE * (uint32_t)sizeof(K));
             if (PAIRS) prefetch_l2_bulk(vsrc + pf * TILE, TILE * (uint32_t)VB);
         }
-        sm.tile = atomicAdd(&hdr->tile_counter[prm.pass], 1u);
     }
-    const uint32_t dbase = (tid < 256) ? prm.digit_base[prm.pass * 256 + tid] : 0u;
+    if (tid == 0) {
+        sm.num_active = A;
+        sm.ordinal = k;
+    }
     for (int i = tid; i < WARPS * 256; i += THREADS) (&sm.whist[0][0])[i] = 0;
     __syncthreads();
     const uint32_t tile = sm.tile;
     const size_t tile_start = (size_t)tile * TILE;
     const uint32_t valid = (uint32_t)min((size_t)TILE, (size_t)prm.n - tile_start);
-    {
-        uint32_t phase = 0;
-        bool have = false;
-        if (spec_ok) {
-            wait_phase(&sm.bar, phase, prm, hdr, tile);  // the speculative copy has landed
-            ++phase;
-            have = (tile == spec);
-        }
-        if (!have) {
-            // every thread must have seen phase 0 complete before phase 1 can
-            // start, or a late poller of parity 0 would wait on phase 2
-            if (spec_ok) __syncthreads();
-            if (valid == TILE && aligned) {
-                if (tid == 0) {
-                    mbar_arrive_expect_tx(&sm.bar, tx_bytes);
-                    bulk_g2s(sm.keys, ksrc + tile_start, TILE * (uint32_t)sizeof(K), &sm.bar);
-                    if (PAIRS) bulk_g2s(sm.vals, vsrc + tile_start, TILE * (uint32_t)VB, &sm.bar);
-                }
-                wait_phase(&sm.bar, phase, prm, hdr, tile);
-            } else {
-                for (uint32_t i = tid; i < valid; i += THREADS) {
-                    sm.keys[i] = ksrc[tile_start + i];
-                    if (PAIRS) sm.vals[i] = vsrc[tile_start + i];
-                }
-                __syncthreads();
-            }
-        }
-    }
-
-    // ---- stable rank within the tile --------------------------------------
-    K keys[ITEMS];
-    PackedRanks<ITEMS> ranks;
-    uint32_t *whist = sm.whist[warp];
-    if (valid == TILE) {
-        if (first)
-            rank_warp<true, BYTE, true>(sm.keys, whist, prm, warp, lane, valid, keys, ranks);
-        else
-            rank_warp<false, BYTE, true>(sm.keys, whist, prm, warp, lane, valid, keys, ranks);
+    if (valid == TILE && aligned) {
+        wait_phase(&sm.bar, 0, prm, hdr, tile);
     } else {
-        if (first)
-            rank_warp<true, BYTE, false>(sm.keys, whist, prm, warp, lane, valid, keys, ranks);
-        else
-            rank_warp<false, BYTE, false>(sm.keys, whist, prm, warp, lane, valid, keys, ranks);
-    }
-    __syncthreads();
-
-    // ---- tile digit counts, warp offsets, publish the aggregate ------------
-    uint32_t cnt = 0;
-    uint32_t *my_status = prm.status + (size_t)tile * 256;
-    const bool faulty = (prm.fault_pass == prm.pass) && (prm.fault_tile == tile);
-    if (tid < 256) {
-        cnt = tile_digit_count<WARPS>(sm.whist, tid);
-        if (!faulty) st_relaxed_gpu(my_status + tid, ((tile == 0 ? st_inc : st_agg) << STATUS_COUNT_BITS) | cnt);
-    }
-    // (wsum is not written again before the barrier after the offsets)
-    const uint32_t local = excl_scan_256<false>(cnt, sm.wsum);
-    if (tid < 256) {
-        // sorted-tile slot of each warp's first key of digit tid
-#pragma unroll 4
-        for (int w = 0; w < WARPS; ++w) sm.whist[w][tid] += local;
-    }
-    __syncthreads();
-
-    // ---- reorder the tile in shared memory by (digit, rank) ---------------
-#pragma unroll
-    for (int i = 0; i < ITEMS; ++i) {
-        const uint32_t idx = (uint32_t)warp * (ITEMS * 32) + i * 32 + lane;
-        if (valid == TILE || idx < valid) {
-            const uint32_t slot = ranks.get(i) + whist[pass_digit<BYTE>(keys[i], prm)];
-            if (PAIRS) ranks.replace(i, slot);
-            sm.keys[slot] = keys[i];
-        }
-    }
-    if (PAIRS) {
-        V vals[ITEMS];
-#pragma unroll
-        for (int i = 0; i < ITEMS; ++i) {
-            const uint32_t idx = (uint32_t)warp * (ITEMS * 32) + i * 32 + lane;
-            vals[i] = (idx < valid) ? sm.vals[idx] : V(0);
+        for (uint32_t i = tid; i < valid; i += THREADS) {
+            sm.keys[i] = ksrc[tile_start + i];
+            if (PAIRS) sm.vals[i] = vsrc[tile_start + i];
         }
         __syncthreads();
-#pragma unroll
-        for (int i = 0; i < ITEMS; ++i) {
-            const uint32_t idx = (uint32_t)warp * (ITEMS * 32) + i * 32 + lane;
-            if (idx < valid) sm.vals[ranks.get(i)] = vals[i];
-        }
     }
 
-    // ---- decoupled look-back over the predecessors' status words ----------
-    // Each digit's thread reads LOOKBACK_WINDOW predecessors per round trip
-    // (registers are free again: the tile's keys now sit in shared memory),
-    // adds the aggregates from the nearest one back to the first inclusive
-    // prefix, and waits (bounded) only at a predecessor that has published
-    // nothing yet.
-    if (tid < 256) {
-        uint32_t excl = 0;
-        if (tile > 0) {
-            excl = lookback_excl(prm, hdr, tile, tid, st_agg, st_inc);
-            if (!faulty)
-                st_relaxed_gpu(my_status + tid, (st_inc << STATUS_COUNT_BITS) | ((excl + cnt) & STATUS_COUNT_MASK));
-        }
-        sm.binoff[tid] = dbase + excl - local;
-    }
-    __syncthreads();
-
-    if (last)
-        store_tile<true, BYTE, K, VB, THREADS>(sm.keys, sm.vals, sm.binoff, valid, kdst, vdst, prm, tid);
+    if (valid == TILE)
+        pass_tile<true, K, VB, THREADS, ITEMS, BYTE>(sm, prm, hdr, valid, first);
     else
-        store_tile<false, BYTE, K, VB, THREADS>(sm.keys, sm.vals, sm.binoff, valid, kdst, vdst, prm, tid);
+        pass_tile<false, K, VB, THREADS, ITEMS, BYTE>(sm, prm, hdr, valid, first);
 }
 
 // ---------------------------------------------------------------------------

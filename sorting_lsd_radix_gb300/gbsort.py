@@ -39,7 +39,7 @@ _KIND_BYTES = {GBS_U32: 4, GBS_I32: 4, GBS_F32: 4, GBS_U64: 8, GBS_I64: 8, GBS_F
 EXPORTS = ("gbs_sort_keys", "gbs_sort_pairs", "gbs_segmented_sort", "gbs_digit_histograms", "gbs_get_status",
            "gbs_status_string", "gbs_version", "gbs_debug_set_lookback_fault", "gbs_debug_last_launch_count",
            "gbs_debug_radix_tile_keys", "gbs_debug_set_timing_events", "gbs_sort_keys_noalloc",
-           "gbs_sort_keys_host", "gbs_segmented_sort_offsets", "gbs_sort_pairs64")
+           "gbs_sort_keys_host", "gbs_segmented_sort_offsets", "gbs_sort_pairs64", "gbs_get_status_noalloc")
 GBS_NOALLOC_MAX_KEYS = 1 << 20
 
 
@@ -79,6 +79,8 @@ def load(path: str | None = None):
     lib.gbs_digit_histograms.restype = i
     lib.gbs_sort_keys_noalloc.argtypes = [i, vp, vp, sz, i, i, i, vp]
     lib.gbs_sort_keys_noalloc.restype = i
+    lib.gbs_get_status_noalloc.argtypes = [vp]
+    lib.gbs_get_status_noalloc.restype = i
     lib.gbs_get_status.argtypes = [vp, sz, vp]
     lib.gbs_get_status.restype = i
     lib.gbs_status_string.argtypes = [i]
@@ -238,8 +240,10 @@ def gbs_sort_pairs(keys_in: torch.Tensor, vals_in: torch.Tensor, keys_out: torch
 
 def gbs_segmented_sort(keys_in: torch.Tensor, num_segments: int, segment_len: int,
                        keys_out: torch.Tensor | None = None, descending: bool = False,
-                       temp: torch.Tensor | None = None, key_type: int | None = None, stream=None):
-    """Bitonic sort of each of num_segments consecutive segments of segment_len keys."""
+                       temp: torch.Tensor | None = None, key_type: int | None = None, stream=None,
+                       return_temp: bool = False):
+    """Sort each of num_segments consecutive segments of segment_len keys (bitonic network up to
+    GBS_MAX_SEGMENT_LEN keys per segment, the radix sort segment by segment above)."""
     kind = _kind(keys_in, key_type)
     n = num_segments * segment_len
     _check_tensor(keys_in, n, "keys_in")
@@ -247,8 +251,8 @@ def gbs_segmented_sort(keys_in: torch.Tensor, num_segments: int, segment_len: in
         keys_out = torch.empty_like(keys_in)
     _check_tensor(keys_out, n, "keys_out")
     args = (kind, _ptr(keys_in), _ptr(keys_out), num_segments, segment_len, int(bool(descending)), _stream(stream))
-    _run(load().gbs_segmented_sort, args, temp, "gbs_segmented_sort")
-    return keys_out
+    temp = _run(load().gbs_segmented_sort, args, temp, "gbs_segmented_sort")
+    return (keys_out, temp) if return_temp else keys_out
 
 
 def gbs_segmented_sort_offsets(keys_in: torch.Tensor, offsets, keys_out: torch.Tensor | None = None,
@@ -313,6 +317,12 @@ def gbs_sort_keys_noalloc(keys_in: torch.Tensor, keys_out: torch.Tensor, begin_b
     if st != GBS_OK:
         raise GbsError(st, "gbs_sort_keys_noalloc")
     return keys_out
+
+
+def gbs_get_status_noalloc(stream=None) -> int:
+    """Synchronises the stream; GBS_ERR_TIMEOUT if the last gbs_sort_keys_noalloc call on the
+    current device timed out."""
+    return load().gbs_get_status_noalloc(_stream(stream))
 
 
 def gbs_get_status(temp: torch.Tensor, stream=None) -> int:

@@ -132,8 +132,12 @@ def test_bad_key_type_and_limits(lib):
     assert _query(lib, "gbs_sort_keys", 6, None, None, 10, 0, 8, 0, None)[0] == gbsort.GBS_ERR_INVALID_ARG
     assert _query(lib, "gbs_sort_keys", gbsort.GBS_U32, None, None, gbsort.GBS_MAX_RADIX_KEYS + 1, 0, 32, 0,
                   None)[0] == gbsort.GBS_ERR_UNSUPPORTED
-    assert _query(lib, "gbs_segmented_sort", gbsort.GBS_U32, None, None, 4, 16385, 0, None)[0] == \
-        gbsort.GBS_ERR_UNSUPPORTED
+    # segments longer than one CTA's network take the radix path: a larger work buffer
+    st_small, need_small = _query(lib, "gbs_segmented_sort", gbsort.GBS_U32, None, None, 4, 16384, 0, None)
+    st_long, need_long = _query(lib, "gbs_segmented_sort", gbsort.GBS_U32, None, None, 4, 16385, 0, None)
+    assert st_small == st_long == gbsort.GBS_OK and need_long > need_small + 4 * 16385
+    assert _query(lib, "gbs_segmented_sort", gbsort.GBS_U32, None, None, 1, gbsort.GBS_MAX_RADIX_KEYS + 1, 0,
+                  None)[0] == gbsort.GBS_ERR_UNSUPPORTED
     assert lib.gbs_sort_keys(None, None, gbsort.GBS_U32, None, None, 10, 0, 32, 0, None) == \
         gbsort.GBS_ERR_INVALID_ARG
 

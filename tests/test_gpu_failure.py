@@ -46,6 +46,6 @@ def test_invalid_arguments_launch_nothing(g):
         g.gbs_sort_keys(t, begin_bit=4, end_bit=2)
     assert e.value.status == g.GBS_ERR_INVALID_ARG
     with pytest.raises(g.GbsError) as e:
-        g.gbs_segmented_sort(torch.zeros(20000, dtype=torch.uint32, device="cuda"), 1, 20000)
-    assert e.value.status == g.GBS_ERR_UNSUPPORTED
+        g.gbs_sort_pairs(t, torch.zeros(100, dtype=torch.uint32, device="cuda"), begin_bit=0, end_bit=33)
+    assert e.value.status == g.GBS_ERR_INVALID_ARG
     assert g.gbs_debug_last_launch_count() == 0

@@ -323,6 +323,24 @@ SEG_MIX = [0, 1, 2, 3, 5, 17, 100, 255, 256, 1000, 1023, 1024, 1025, 2047, 4097,
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("seg_len", [16385, 40000, 65537])
+def test_segmented_sort_long_segments(g, dtype, seg_len):
+    """Fixed-length segments above one CTA's network take the radix path, segment by segment."""
+    segs = 3
+    keys = sample(dtype, segs * seg_len, seg_len) if seg_len != 40000 else with_ties(dtype, segs * seg_len, seg_len)
+    for desc in (False, True):
+        got = _host(g.gbs_segmented_sort(_dev(keys), segs, seg_len, descending=desc))
+        want = np.concatenate([oracle.sort_keys(keys[i * seg_len:(i + 1) * seg_len], descending=desc)
+                               for i in range(segs)])
+        assert np.array_equal(_u(got), _u(want)), desc
+    t = _dev(keys)
+    out, temp = g.gbs_segmented_sort(t, segs, seg_len, keys_out=t, return_temp=True)  # in place
+    assert g.gbs_get_status(temp) == g.GBS_OK
+    want = np.concatenate([oracle.sort_keys(keys[i * seg_len:(i + 1) * seg_len]) for i in range(segs)])
+    assert np.array_equal(_u(_host(t)), _u(want))
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("desc", [False, True])
 @pytest.mark.parametrize("in_place", [False, True])
 def test_segmented_sort_offsets(g, dtype, desc, in_place):
