@@ -34,8 +34,8 @@ METRIC = "uint32 keys sorted/s at n=1e8; achieved HBM GB/s vs GB300 peak"
 UNIT = "keys/s"
 WORKLOAD = "sort_keys u32 ascending, bits [0,32), n=1e8 i.i.d. uniform keys (SplitMix64)"
 FALLBACK_HBM_GBS = 6800.0
-PASS_KERNEL_SOURCES = ["sorting_lsd_radix_gb300/csrc/radix.cu", "sorting_lsd_radix_gb300/csrc/common.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "onesweep_pass_u32_2p26.md")
+PASS_KERNEL_SOURCES = ["sorting_lsd_radix_gb300/csrc/radix_impl.cuh", "sorting_lsd_radix_gb300/csrc/common.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "onesweep_pass_u32_traffic.json")
 
 
 def parse():
@@ -88,24 +88,16 @@ def source_hash():
 
 
 def recorded_traffic(n):
-    """DRAM bytes per pass-kernel launch from the committed ncu summary, scaled to n keys
-    (traffic grows in proportion to n); None if absent or taken on a different kernel source."""
+    """DRAM bytes per pass-kernel launch from the committed ncu record (profiles/*.json), scaled to
+    n keys (traffic grows in proportion to n); None if absent or taken on a different kernel source."""
     try:
-        lines = open(TRAFFIC_FILE).read().splitlines()
-    except OSError:
-        return None
-    rec = {}
-    for ln in lines:
-        if ":" in ln:
-            k, v = ln.split(":", 1)
-            rec[k.strip()] = v.split()
-    try:
-        if rec["source_sha256_16"][0] != source_hash():
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+        if rec["source_sha256_16"] != source_hash():
             return None
-        n_cap, bytes_cap = (float(x) for x in rec["traffic_bytes_per_launch_at_n"][:2])
-    except (KeyError, ValueError, IndexError):
+        return float(rec["dram_bytes_per_launch"]) * n / float(rec["n"])
+    except (OSError, KeyError, ValueError, TypeError):
         return None
-    return bytes_cap * n / n_cap
 
 
 class ClockSampler:
@@ -189,7 +181,7 @@ def cpu_baseline(n_total, seconds=10.0):
         if time.perf_counter() > t_end or len(times) >= 20:
             break
     med = statistics.median(times)
-    return {"value": sample_n / med, "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": sample_n / med, "unit": UNIT, "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle",
             "sample": f"first {sample_n} keys of the workload (same generator and seed), serial LSD radix sort, "
                       f"median of {len(times)} runs",
             "library_sort": library_sort_baseline(keys)}
@@ -230,7 +222,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic",
             "config": {"workload": WORKLOAD, "n": args.n, "step_sample_keys": sample_n},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle",
                              "sample": f"first {sample_n} keys of the workload per step, serial LSD radix sort"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -442,26 +434,11 @@ def run_gbsort(args):
 # dominant-kernel launch indices, extra fields).
 # ---------------------------------------------------------------------------
 
-def _active_passes(keys, begin, end):
+def _active_passes(gbsort, d_keys, begin, end, desc):
     """Digit passes whose digit is not the same for every key (a pass with one digit value moves
-    nothing and is skipped by the sort).  Bench bookkeeping for the traffic figure: the sort order
-    of a pass does not depend on the key code's sign handling, only which digit values occur."""
-    u = keys.view(np.uint64 if keys.itemsize == 8 else np.uint32)
-    if keys.dtype == np.float32:
-        u = u ^ np.where(u >> np.uint32(31), np.uint32(0xFFFFFFFF), np.uint32(0x80000000))
-    elif keys.dtype == np.int32:
-        u = u ^ np.uint32(0x80000000)
-    elif keys.dtype == np.float64:
-        u = u ^ np.where(u >> np.uint64(63), np.uint64(2**64 - 1), np.uint64(2**63))
-    elif keys.dtype == np.int64:
-        u = u ^ np.uint64(2**63)
-    act = []
-    for p, lo in enumerate(range(begin, end, 8)):
-        mask = u.dtype.type((1 << min(8, end - lo)) - 1)
-        dig = (u >> u.dtype.type(lo)) & mask
-        if dig.min() != dig.max():
-            act.append(p)
-    return act
+    nothing and is skipped by the sort), from the library's own upfront-histogram kernel."""
+    hist = gbsort.gbs_digit_histograms(d_keys, begin_bit=begin, end_bit=end, descending=desc).cpu().numpy()
+    return [p for p in range(hist.shape[0]) if np.count_nonzero(hist[p]) > 1]
 
 
 def _sec_radix_keys(gen, n_default, key_type, begin=0, end=None, desc=False):
@@ -474,13 +451,14 @@ def _sec_radix_keys(gen, n_default, key_type, begin=0, end=None, desc=False):
         s = keys.itemsize
         stop = end if end is not None else 8 * s
         passes = (stop - begin + 7) // 8
-        active = _active_passes(keys, begin, stop)
+        active = _active_passes(gbsort, d, begin, stop, desc)
         # histogram read + one read and one write per active pass (all trivial: the last pass
         # launch copies the keys once)
         alg = s * n + max(len(active), 1) * 2 * s * n
         dom = [1 + p for p in active] if active else [passes]
         call = lambda: gbsort.gbs_sort_keys(d, o, begin_bit=begin, end_bit=end, descending=desc, temp=temp)
-        return call, temp, n, alg, 2 * s * n, dom, {"active_passes": len(active)}
+        return call, temp, n, alg, 2 * s * n, dom, {"active_passes": len(active),
+                                                    "oracle_sample": (keys, begin, stop, desc)}
     return build
 
 
@@ -500,8 +478,9 @@ def _sec_radix_graph(n):
     return build
 
 
-def _sec_pairs_u64(n):
-    def build(gbsort, torch):
+def _sec_pairs_u64(n_default):
+    def build(gbsort, torch, n=None):
+        n = n or n_default
         keys = wl.priority_u64(n, wl.seed_for(4, 0))
         d = torch.from_numpy(keys).cuda()
         v = torch.arange(n, dtype=torch.int32, device="cuda").view(torch.uint32)
@@ -544,6 +523,23 @@ def _sec_segmented_var(num_segments, max_len):
     return build
 
 
+def _sec_msd_bitonic(n_default):
+    """The hybrid prototype: MSD radix passes over the top 16 bits, then a bitonic sort per bucket."""
+    def build(gbsort, torch, n=None):
+        n = n or n_default
+        keys = wl.uniform_u32(n, SEED)
+        d = torch.from_numpy(keys).cuda()
+        o = torch.empty_like(d)
+        _, temp = gbsort.gbs_sort_keys_msd_bitonic(d, o, return_temp=True)
+        call = lambda: gbsort.gbs_sort_keys_msd_bitonic(d, o, temp=temp)
+        launches = gbsort.gbs_debug_last_launch_count()
+        # two MSD passes (histogram read + 2 x (read + write)), the boundary scan (one read) and the
+        # bitonic finish (one read and one write)
+        return call, temp, n, 4 * n + 2 * 8 * n + 4 * n + 8 * n, 8 * n, list(range(launches)), \
+            {"sum_dominant": True, "hybrid": "MSD 16 bits + bitonic per bucket"}
+    return build
+
+
 SECONDARY = {
     "u32_2p20": ("sort_keys u32 n=2^20 uniform (L2-resident: launch-latency bound, roofline not meaningful)",
                  _sec_radix_keys(lambda n: wl.uniform_u32(n, wl.seed_for(1, 0)), 1 << 20, "u32")),
@@ -557,6 +553,8 @@ SECONDARY = {
                         _sec_radix_keys(lambda n: wl.descending_u32(n, wl.seed_for(3, 1)), N_KEYS, "u32")),
     "u32_1e8_all_equal": ("sort_keys u32 n=1e8, all keys equal (every pass trivial: histogram + copy)",
                           _sec_radix_keys(lambda n: wl.all_equal_u32(n, wl.seed_for(3, 1)), N_KEYS, "u32")),
+    "u32_1e8_msd_bitonic": ("sort_keys u32 n=1e8 uniform by the hybrid prototype: MSD radix over the top 16 bits, "
+                            "then a bitonic sort of each of the 65536 buckets", _sec_msd_bitonic(N_KEYS)),
     "u32_1e8_bits0_16": ("sort_keys u32 n=1e8 uniform, bits [0,16)",
                          _sec_radix_keys(lambda n: wl.uniform_u32(n, SEED), N_KEYS, "u32", 0, 16)),
     "f32_2p28": ("sort_keys f32 n=2^28, N(0,1000) with signed zeros and infinities",
@@ -577,6 +575,23 @@ SECONDARY = {
     "segvar_16384x1to2048": ("segmented_sort_offsets u32, 16384 segments of 1..2048 keys (uniform lengths)",
                              _sec_segmented_var(16384, 2048)),
 }
+
+
+def secondary_cpu_baseline(keys, begin, end, desc, seconds=10.0):
+    """The oracle, single-threaded, on the first (up to) 2^22 keys of a secondary workload."""
+    import oracle
+    sample = np.ascontiguousarray(keys[: 1 << 22])
+    times = []
+    t_end = time.perf_counter() + seconds
+    while True:
+        t0 = time.perf_counter()
+        oracle.sort_keys(sample, begin, end, descending=desc)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() > t_end or len(times) >= 5:
+            break
+    med = statistics.median(times)
+    return {"value": sample.size / med, "unit": UNIT, "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {sample.size} keys of the workload, median of {len(times)} runs"}
 
 
 def run_secondary(args):
@@ -633,9 +648,12 @@ def run_secondary(args):
             "kernel_ms": per_kernel.tolist(), "launches": launches}
     if "comparators_per_call" in extra:
         line["comparators_per_s"] = extra["comparators_per_call"] / (ms / 1e3)
+    sample = extra.pop("oracle_sample", None)
     line.update({k: v for k, v in extra.items() if k != "comparators_per_call"})
     if temp is not None:
         line["status"] = gbsort.status_string(gbsort.gbs_get_status(temp))
+    if sample is not None and not args.no_cpu_baseline:
+        line["cpu_baseline"] = secondary_cpu_baseline(*sample)
     print(json.dumps(line), flush=True)
 
 

@@ -69,9 +69,11 @@ typedef enum {
                     infinities at the extremes, a NaN by its bits */
 } gbs_key_type;
 
-/* Largest number of keys a radix sort call accepts: per-digit counts are
- * kept in 29-bit fields of the tile status words. */
-#define GBS_MAX_RADIX_KEYS ((size_t)((1u << 29) - 1))
+/* Largest number of keys a radix sort call accepts: keys, positions and
+ * per-digit counts are 32-bit.  Sorts of 2^29 keys or more keep their
+ * look-back status in 64-bit words (about 2 KiB per 8192-key tile instead of
+ * 1 KiB, which the work-buffer size query includes). */
+#define GBS_MAX_RADIX_KEYS ((size_t)0xFFFFFFFFu)
 /* Longest segment that one CTA's bitonic network sorts on chip; longer
  * segments take the radix path. */
 #define GBS_MAX_SEGMENT_LEN ((size_t)16384)
@@ -181,6 +183,23 @@ gbs_status gbs_segmented_sort(void *d_temp, size_t *temp_bytes, gbs_key_type key
 gbs_status gbs_segmented_sort_offsets(void *d_temp, size_t *temp_bytes, gbs_key_type key_type, const void *d_keys_in,
                                       void *d_keys_out, size_t num_segments, const uint64_t *h_offsets,
                                       int descending, void *stream);
+
+/*
+ * gbs_sort_keys_msd_bitonic — gbs_sort_keys over the full key width (same
+ * key types, order and result) by the pages' hybrid: most-significant-digit
+ * radix passes group the keys by the top 16 bits of their code into 65536
+ * buckets, then the bitonic network sorts every bucket on chip, each padded
+ * only to its own power of two (kwkr.cn notes §5.3: bucket by the high bits,
+ * bitonic-sort each bucket; §3.4 and §5.2 on cutting radix passes).  Keys
+ * only, full width; buckets above GBS_MAX_SEGMENT_LEN keys take the radix
+ * path.  A measured alternative to gbs_sort_keys, not its replacement.
+ * Unlike the other entry points it synchronises `stream` once (the bucket
+ * plan is made on the host).  Same work-buffer protocol; device-side
+ * timeouts are reported by the return value or by gbs_get_status.
+ */
+gbs_status gbs_sort_keys_msd_bitonic(void *d_temp, size_t *temp_bytes, gbs_key_type key_type,
+                                     const void *d_keys_in, void *d_keys_out, size_t n,
+                                     int descending, void *stream);
 
 /*
  * gbs_digit_histograms — the upfront digit histograms of a radix sort on

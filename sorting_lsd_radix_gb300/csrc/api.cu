@@ -62,7 +62,7 @@ Layout radix_layout(int key_bytes, int val_bytes, size_t n) {
     l.digit_base = off;
     off += round_up(sizeof(uint32_t) * gbs::MAX_PASSES * 256);
     l.status = off;
-    off += round_up(sizeof(uint32_t) * 256 * (size_t)l.num_tiles);
+    off += round_up(gbs::status_bytes(n, l.num_tiles));
     l.keys_alt = off;
     off += round_up((size_t)key_bytes * n);
     l.vals_alt = off;
@@ -149,7 +149,8 @@ gbs_status radix_common(void *d_temp, size_t *temp_bytes, gbs_key_type kt, const
     job.hdr = reinterpret_cast<Header *>(tb);
     job.hist = reinterpret_cast<uint32_t *>(tb + lay.hist);
     job.digit_base = reinterpret_cast<uint32_t *>(tb + lay.digit_base);
-    job.status = reinterpret_cast<uint32_t *>(tb + lay.status);
+    job.status = tb + lay.status;
+    job.wide_status = n >= gbs::WIDE_STATUS_MIN_KEYS;
     job.num_tiles = lay.num_tiles;
     job.spin_limit = g_spin_limit;
     job.fault_pass = g_fault_pass;
@@ -173,7 +174,7 @@ void timing_mark(cudaStream_t s) {
 }
 }  // namespace gbs
 
-static_assert(GBS_MAX_RADIX_KEYS == gbs::STATUS_COUNT_MASK, "key limit must match the status count field");
+static_assert(GBS_MAX_RADIX_KEYS <= gbs::StatusWord<uint64_t>::MAX_KEYS, "key limit must fit the status words");
 static_assert((int)GBS_U32 == gbs::KIND_U32 && (int)GBS_I32 == gbs::KIND_I32 && (int)GBS_F32 == gbs::KIND_F32 &&
                   (int)GBS_U64 == gbs::KIND_U64 && (int)GBS_I64 == gbs::KIND_I64 && (int)GBS_F64 == gbs::KIND_F64,
               "the ABI's key types are the kernels' key kinds");
@@ -361,6 +362,57 @@ gbs_status gbs_segmented_sort_offsets(void *d_temp, size_t *temp_bytes, gbs_key_
         if (st != GBS_OK) return st;
     }
     return GBS_OK;
+}
+
+gbs_status gbs_sort_keys_msd_bitonic(void *d_temp, size_t *temp_bytes, gbs_key_type key_type, const void *d_keys_in,
+                                     void *d_keys_out, size_t n, int descending, void *stream) {
+    const int kb = key_bytes_of(key_type);
+    if (kb == 0 || temp_bytes == nullptr) return GBS_ERR_INVALID_ARG;
+    if (n > GBS_MAX_RADIX_KEYS) return GBS_ERR_UNSUPPORTED;
+    constexpr size_t BUCKETS = 65536;
+    // work buffer: [radix sort of n keys | the segment sort's own work area] [bucket bounds]; the
+    // segment sort needs at most a radix area for its longest segment (<= n keys), its offsets
+    // and its segment list
+    size_t radix_bytes = 0;
+    gbs_status st = radix_common(nullptr, &radix_bytes, key_type, nullptr, nullptr, nullptr, nullptr, 0, n, 0, 8 * kb,
+                                 descending, stream);
+    if (st != GBS_OK) return st;
+    const size_t seg_bytes = round_up(radix_bytes) + round_up(sizeof(uint64_t) * (BUCKETS + 1)) +
+                             round_up(sizeof(uint32_t) * BUCKETS);
+    const size_t off_bounds = round_up(seg_bytes);
+    bool query = false;
+    st = check_temp(d_temp, temp_bytes, off_bounds + round_up(sizeof(uint64_t) * (BUCKETS + 1)), &query);
+    if (st != GBS_OK || query) return st;
+    if (n > 0 && (d_keys_in == nullptr || d_keys_out == nullptr)) return GBS_ERR_INVALID_ARG;
+    if (n <= GBS_MAX_SEGMENT_LEN)  // one segment: the regular entry point (one bitonic CTA)
+        return gbs_sort_keys(d_temp, temp_bytes, key_type, d_keys_in, d_keys_out, n, 0, 8 * kb, descending, stream);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // 1. MSD: stable radix passes over the top 16 bits of the code (two 8-bit digits)
+    size_t have = radix_bytes;
+    st = radix_common(d_temp, &have, key_type, d_keys_in, d_keys_out, nullptr, nullptr, 0, n, 8 * kb - 16, 8 * kb,
+                      descending, stream);
+    if (st != GBS_OK) return st;
+    int launches = t_launches;
+    // 2. bucket boundaries, copied to the host for the per-bucket plan (this synchronises)
+    uint64_t *d_bounds = reinterpret_cast<uint64_t *>(static_cast<unsigned char *>(d_temp) + off_bounds);
+    if (gbs::launch_bucket_bounds((int)key_type, kb, d_keys_out, n, descending != 0, d_bounds, s, &launches) !=
+        cudaSuccess)
+        return GBS_ERR_CUDA;
+    std::vector<uint64_t> bounds(BUCKETS + 1);
+    if (cudaMemcpyAsync(bounds.data(), d_bounds, sizeof(uint64_t) * (BUCKETS + 1), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return GBS_ERR_CUDA;
+    uint32_t err = 0;  // a timeout of the MSD passes is reported like the sort's own
+    if (cudaMemcpy(&err, d_temp, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess) return GBS_ERR_CUDA;
+    if (err) return GBS_ERR_TIMEOUT;
+    // 3. every bucket sorted in place by the bitonic network, padded to its own power of two
+    //    (buckets above 2^14 keys: the radix path)
+    have = seg_bytes;
+    st = gbs_segmented_sort_offsets(d_temp, &have, key_type, d_keys_out, d_keys_out, BUCKETS, bounds.data(),
+                                    descending, stream);
+    t_launches += launches;
+    return st;
 }
 
 gbs_status gbs_digit_histograms(void *d_temp, size_t *temp_bytes, gbs_key_type key_type, const void *d_keys,

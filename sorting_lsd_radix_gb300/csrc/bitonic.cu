@@ -406,3 +406,41 @@ cudaError_t launch_segmented_bitonic(int kind, int key_bytes, const void *keys_i
 }
 
 }  // namespace gbs
+
+// ---------------------------------------------------------------------------
+// Bucket boundaries of keys sorted by the top 16 bits of their code (the
+// MSD-then-bitonic prototype): bounds[c] = first position whose bucket is at
+// least c, for c = 0 .. 65536 (bounds[65536] = n).  Position i writes the
+// boundaries of every bucket in (bucket(i-1), bucket(i)], so each of the
+// 65537 entries is written exactly once.
+// ---------------------------------------------------------------------------
+namespace gbs {
+namespace {
+
+template <typename K>
+__global__ void bucket_bounds_kernel(const K *keys, size_t n, int kind, K flip, int shift, uint64_t *bounds) {
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i <= n; i += stride) {
+        const int64_t b = (i < n) ? (int64_t)(KeyCodec<K>::enc(keys[i], kind, flip) >> shift) : 65536;
+        const int64_t prev = (i > 0) ? (int64_t)(KeyCodec<K>::enc(keys[i - 1], kind, flip) >> shift) : -1;
+        for (int64_t c = prev + 1; c <= b; ++c) bounds[c] = i;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_bucket_bounds(int kind, int key_bytes, const void *keys, size_t n, bool descending,
+                                 uint64_t *bounds, cudaStream_t stream, int *launches) {
+    const size_t blocks = std::min<size_t>((n + 1 + 255) / 256, 4096);
+    if (key_bytes == 8)
+        bucket_bounds_kernel<uint64_t><<<(unsigned)blocks, 256, 0, stream>>>(
+            reinterpret_cast<const uint64_t *>(keys), n, kind, descending ? ~0ull : 0ull, 48, bounds);
+    else
+        bucket_bounds_kernel<uint32_t><<<(unsigned)blocks, 256, 0, stream>>>(
+            reinterpret_cast<const uint32_t *>(keys), n, kind, descending ? 0xFFFFFFFFu : 0u, 16, bounds);
+    ++*launches;
+    timing_mark(stream);
+    return cudaGetLastError();
+}
+
+}  // namespace gbs

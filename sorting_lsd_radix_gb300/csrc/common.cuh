@@ -122,13 +122,25 @@ struct alignas(256) Header {
 };
 static_assert(sizeof(Header) == 256, "header must be 256 bytes");
 
-// Tile status word of the chained scan: state in bits 29..31, count in 0..28.
-// Active pass with ordinal k uses states AGG = 1 + 2(k mod 3) (tile count
-// only) and INC = 2 + 2(k mod 3) (inclusive prefix).  Consecutive active
-// passes therefore never mistake each other's words for their own, so the
-// status array is zeroed once per call and then reused by every pass.
-constexpr uint32_t STATUS_COUNT_BITS = 29;
-constexpr uint32_t STATUS_COUNT_MASK = (1u << STATUS_COUNT_BITS) - 1;
+// Tile status word of the chained scan: a 3-bit state in the top bits, a
+// count below.  Active pass with ordinal k uses states AGG = 1 + 2(k mod 3)
+// (tile count only) and INC = 2 + 2(k mod 3) (inclusive prefix).
+// Consecutive active passes therefore never mistake each other's words for
+// their own, so the status array is zeroed once per call and then reused by
+// every pass.  32-bit words (29-bit counts) serve sorts of fewer than 2^29
+// keys; larger sorts use 64-bit words (61-bit counts), which hold any
+// prefix of up to 2^32 - 1 keys.
+template <typename SW> struct StatusWord;
+template <> struct StatusWord<uint32_t> {
+    static constexpr int COUNT_BITS = 29;
+    static constexpr uint32_t COUNT_MASK = (1u << COUNT_BITS) - 1;
+    static constexpr uint64_t MAX_KEYS = COUNT_MASK;  // largest prefix a word holds
+};
+template <> struct StatusWord<uint64_t> {
+    static constexpr int COUNT_BITS = 61;
+    static constexpr uint64_t COUNT_MASK = (1ull << COUNT_BITS) - 1;
+    static constexpr uint64_t MAX_KEYS = 0xFFFFFFFFull;  // keys are counted in 32 bits elsewhere
+};
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -172,6 +184,16 @@ __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p) {
 
 __device__ __forceinline__ void st_relaxed_gpu(uint32_t *p, uint32_t v) {
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed_gpu(const uint64_t *p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu(uint64_t *p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {

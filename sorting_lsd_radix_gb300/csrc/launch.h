@@ -9,6 +9,20 @@
 #include "common.cuh"
 
 namespace gbs {
+// Sorts of at least this many keys use 64-bit look-back status words.
+constexpr size_t WIDE_STATUS_MIN_KEYS = (size_t)StatusWord<uint32_t>::MAX_KEYS + 1;
+// Bytes of look-back status words of a sort of n keys in num_tiles tiles.
+constexpr size_t status_bytes(size_t n, size_t num_tiles) {
+    return num_tiles * 256 * (n >= WIDE_STATUS_MIN_KEYS ? sizeof(uint64_t) : sizeof(uint32_t));
+}
+// Boundaries of the 65536 buckets of the top 16 code bits in keys sorted by
+// them: bounds[c] = first position of bucket c or a later one (65537 words).
+cudaError_t launch_bucket_bounds(int kind, int key_bytes, const void *keys, size_t n, bool descending,
+                                 uint64_t *bounds, cudaStream_t stream, int *launches);
+
+}  // namespace gbs
+
+namespace gbs {
 
 // One-time set-up of a kernel (its shared-memory attribute), done once per
 // device: the first launch on each device runs `setup`; a set-up that fails
@@ -49,7 +63,8 @@ struct RadixJob {
     Header *hdr;
     uint32_t *hist;        // [MAX_PASSES][256]
     uint32_t *digit_base;  // [MAX_PASSES][256]
-    uint32_t *status;      // [num_tiles][256]
+    void *status;          // [num_tiles][256] status words
+    bool wide_status;      // 64-bit status words (sorts of 2^29 keys or more), else 32-bit
     uint32_t num_tiles;
     uint32_t spin_limit;   // bounded look-back wait (polls)
     int fault_pass;        // test hook: tile fault_tile of pass fault_pass never publishes (-1: off)
@@ -68,6 +83,9 @@ void timing_mark(cudaStream_t stream);
 // value width (0: keys only).
 uint32_t radix_tile_keys(int key_bytes, int val_bytes);
 
+// The digit passes of a job with 64-bit look-back status words (radix_wide.cu).
+cudaError_t launch_passes_wide(const RadixJob &job, cudaStream_t stream, int *launches);
+
 // Histogram + plan, then every digit pass (and the final copy when needed).
 cudaError_t launch_radix_sort(const RadixJob &job, cudaStream_t stream, int *launches);
 
@@ -83,5 +101,10 @@ cudaError_t launch_segmented_bitonic(int kind, int key_bytes, const void *keys_i
 cudaError_t launch_listed_bitonic(int kind, int key_bytes, const void *keys_in, void *keys_out,
                                   const uint32_t *seg_ids, size_t count, const uint64_t *offsets, int len_log,
                                   bool descending, cudaStream_t stream, int *launches);
+
+// Boundaries of the 65536 buckets of the top 16 code bits in keys sorted by
+// them: bounds[c] = first position of bucket c or a later one (65537 words).
+cudaError_t launch_bucket_bounds(int kind, int key_bytes, const void *keys, size_t n, bool descending,
+                                 uint64_t *bounds, cudaStream_t stream, int *launches);
 
 }  // namespace gbs

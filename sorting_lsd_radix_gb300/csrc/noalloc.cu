@@ -29,6 +29,8 @@ constexpr size_t kStatus = kMaxTiles * 256 * 4;
 constexpr size_t kKeys = (size_t)GBS_NOALLOC_MAX_KEYS * 8;
 constexpr size_t kScratchBytes = kHeader + 2 * kHist + kStatus + kKeys;
 
+static_assert(kStatus == gbs::status_bytes(GBS_NOALLOC_MAX_KEYS, kMaxTiles),
+              "scratch must hold the look-back status of its largest sort");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 // Device address of g_noalloc_scratch on the current device.  In host code
@@ -68,7 +70,7 @@ extern "C" gbs_status gbs_sort_keys_noalloc(gbs_key_type key_type, const void *d
     const uint32_t tile = gbs::radix_tile_keys(kb, 0);
     const uint32_t tiles = (uint32_t)((n + tile - 1) / tile);
     const size_t off_hist = kHeader, off_base = off_hist + kHist, off_status = off_base + kHist;
-    const size_t off_keys = off_status + up((size_t)tiles * 256 * 4);
+    const size_t off_keys = off_status + up(gbs::status_bytes(n, tiles));
     if (off_keys + (size_t)kb * n > kScratchBytes) return GBS_ERR_UNSUPPORTED;
 
     // the header and histograms must start at zero on every call (the
@@ -101,7 +103,8 @@ extern "C" gbs_status gbs_sort_keys_noalloc(gbs_key_type key_type, const void *d
     job.hdr = reinterpret_cast<gbs::Header *>(scratch);
     job.hist = reinterpret_cast<uint32_t *>(scratch + off_hist);
     job.digit_base = reinterpret_cast<uint32_t *>(scratch + off_base);
-    job.status = reinterpret_cast<uint32_t *>(scratch + off_status);
+    job.status = scratch + off_status;
+    job.wide_status = false;  // n <= GBS_NOALLOC_MAX_KEYS, far below the 64-bit status threshold
     job.num_tiles = tiles;
     gbs::debug_fault_settings(&job.fault_pass, &job.fault_tile, &job.spin_limit);
     int launches = 0;

@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_PKG, "libgbsort.so")
 
 GBS_OK, GBS_ERR_INVALID_ARG, GBS_ERR_TEMP_TOO_SMALL, GBS_ERR_UNSUPPORTED, GBS_ERR_CUDA, GBS_ERR_TIMEOUT = range(6)
 GBS_U32, GBS_I32, GBS_F32, GBS_U64, GBS_I64, GBS_F64 = range(6)
-GBS_MAX_RADIX_KEYS = (1 << 29) - 1
+GBS_MAX_RADIX_KEYS = (1 << 32) - 1
 GBS_MAX_SEGMENT_LEN = 16384
 
 _DTYPE_KIND = {
@@ -39,7 +39,8 @@ _KIND_BYTES = {GBS_U32: 4, GBS_I32: 4, GBS_F32: 4, GBS_U64: 8, GBS_I64: 8, GBS_F
 EXPORTS = ("gbs_sort_keys", "gbs_sort_pairs", "gbs_segmented_sort", "gbs_digit_histograms", "gbs_get_status",
            "gbs_status_string", "gbs_version", "gbs_debug_set_lookback_fault", "gbs_debug_last_launch_count",
            "gbs_debug_radix_tile_keys", "gbs_debug_set_timing_events", "gbs_sort_keys_noalloc",
-           "gbs_sort_keys_host", "gbs_segmented_sort_offsets", "gbs_sort_pairs64", "gbs_get_status_noalloc")
+           "gbs_sort_keys_host", "gbs_segmented_sort_offsets", "gbs_sort_pairs64", "gbs_get_status_noalloc",
+           "gbs_sort_keys_msd_bitonic")
 GBS_NOALLOC_MAX_KEYS = 1 << 20
 
 
@@ -79,6 +80,8 @@ def load(path: str | None = None):
     lib.gbs_digit_histograms.restype = i
     lib.gbs_sort_keys_noalloc.argtypes = [i, vp, vp, sz, i, i, i, vp]
     lib.gbs_sort_keys_noalloc.restype = i
+    lib.gbs_sort_keys_msd_bitonic.argtypes = [vp, szp, i, vp, vp, sz, i, vp]
+    lib.gbs_sort_keys_msd_bitonic.restype = i
     lib.gbs_get_status_noalloc.argtypes = [vp]
     lib.gbs_get_status_noalloc.restype = i
     lib.gbs_get_status.argtypes = [vp, sz, vp]
@@ -188,6 +191,22 @@ def gbs_sort_keys(keys_in: torch.Tensor, keys_out: torch.Tensor | None = None, b
         end_bit = 8 * _KIND_BYTES[kind]
     args = (kind, _ptr(keys_in), _ptr(keys_out), n, begin_bit, end_bit, int(bool(descending)), _stream(stream))
     temp = _run(load().gbs_sort_keys, args, temp, "gbs_sort_keys")
+    return (keys_out, temp) if return_temp else keys_out
+
+
+def gbs_sort_keys_msd_bitonic(keys_in: torch.Tensor, keys_out: torch.Tensor | None = None,
+                              descending: bool = False, temp: torch.Tensor | None = None,
+                              key_type: int | None = None, stream=None, return_temp: bool = False):
+    """Full-width key sort by MSD radix passes over the top 16 bits, then a bitonic sort of every
+    bucket (the pages' hybrid; synchronises the stream once)."""
+    kind = _kind(keys_in, key_type)
+    n = keys_in.numel()
+    _check_tensor(keys_in, n, "keys_in")
+    if keys_out is None:
+        keys_out = torch.empty_like(keys_in)
+    _check_tensor(keys_out, n, "keys_out")
+    args = (kind, _ptr(keys_in), _ptr(keys_out), n, int(bool(descending)), _stream(stream))
+    temp = _run(load().gbs_sort_keys_msd_bitonic, args, temp, "gbs_sort_keys_msd_bitonic")
     return (keys_out, temp) if return_temp else keys_out
 
 

@@ -100,9 +100,24 @@ def test_pin_rate_peak_and_library_sort_side_baseline():
     assert side["unit"] == "keys/s" and side["value"] > 0 and side["cores"] == 1
 
 
-def test_recorded_traffic_tracks_the_pass_kernel_source():
-    """The committed ncu summary carries a hash of the pass kernel's sources; the bench reports its
-    DRAM traffic (scaled from 2^26 keys) only while that hash matches."""
+def test_recorded_traffic_tracks_the_pass_kernel_source(tmp_path, monkeypatch):
+    """The committed ncu record (profiles/*.json) carries a hash of the pass kernel's sources; the
+    bench reports its DRAM traffic, scaled to n keys, only while that hash matches."""
+    b = _bench()
+    rec = {"kernel": "onesweep_pass_kernel", "n": 1 << 26, "dram_bytes_per_launch": 500_000_000,
+           "source_sha256_16": b.source_hash()}
+    f = tmp_path / "traffic.json"
+    f.write_text(json.dumps(rec))
+    monkeypatch.setattr(b, "TRAFFIC_FILE", str(f))
+    assert b.recorded_traffic(1 << 27) == pytest.approx(1e9)
+    rec["source_sha256_16"] = "0" * 16  # another kernel source: no traffic figure
+    f.write_text(json.dumps(rec))
+    assert b.recorded_traffic(1 << 26) is None
+    monkeypatch.setattr(b, "TRAFFIC_FILE", str(tmp_path / "missing.json"))
+    assert b.recorded_traffic(1 << 26) is None
+
+
+def test_committed_traffic_record_is_plausible():
     b = _bench()
     rec = b.recorded_traffic(1 << 26)
     if rec is None:

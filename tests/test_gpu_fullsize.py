@@ -114,10 +114,31 @@ def test_config5_2p28(g, kind, desc):
 
 
 @pytest.mark.parametrize("dist", ["uniform", "all_equal"])
-def test_largest_accepted_size_u32(g, dist):
-    # GBS_MAX_RADIX_KEYS keys: the tile status words' 29-bit counts reach their limit (all-equal keys
-    # put every key in one digit; uniform keys make the largest prefixes near n)
-    n = g.GBS_MAX_RADIX_KEYS
+def test_largest_narrow_status_size_u32(g, dist):
+    # 2^29 - 1 keys, the largest sort whose look-back status words are 32-bit: their 29-bit
+    # counts reach the limit (all-equal keys put every key in one digit; uniform keys make the
+    # largest prefixes near n)
+    n = (1 << 29) - 1
     keys = wl.uniform_u32(n, wl.seed_for(3, 7)) if dist == "uniform" else wl.all_equal_u32(n, wl.seed_for(3, 8))
     got = _sorted_u32(g, keys)
     assert np.array_equal(got, oracle.sort_keys(keys))
+
+
+@pytest.mark.parametrize("dist", ["uniform", "all_equal", "and4"])
+def test_wide_status_2p30_plus_7_u32(g, dist):
+    # 2^30 + 7 keys take the 64-bit status words.  "and4": the AND of four uniform draws, so
+    # digit value 0 holds about 60% of the keys in every pass and the inclusive prefixes of
+    # that digit pass 2^29 while every pass stays active
+    n = (1 << 30) + 7
+    if dist == "uniform":
+        keys = wl.uniform_u32(n, wl.seed_for(3, 9))
+    elif dist == "all_equal":
+        keys = wl.all_equal_u32(n, wl.seed_for(3, 10))
+    else:
+        keys = wl.low_entropy_u32(n, wl.seed_for(3, 11))
+        keys &= wl.uniform_u32(n, wl.seed_for(3, 12))
+    got = _sorted_u32(g, keys)
+    want = oracle.sort_keys(keys)
+    if dist == "and4":
+        assert ((want & np.uint32(0xFF)) == 0).sum() > (1 << 29)  # digit 0 of pass 0 passes 2^29 keys
+    assert np.array_equal(got, want)

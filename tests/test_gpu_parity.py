@@ -323,6 +323,29 @@ SEG_MIX = [0, 1, 2, 3, 5, 17, 100, 255, 256, 1000, 1023, 1024, 1025, 2047, 4097,
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("n", [16385, 100003, 1 << 21])
+def test_msd_bitonic_hybrid(g, dtype, n):
+    """MSD radix passes over the top 16 code bits, then a bitonic sort of every bucket: the
+    result is the full-width sort (ties are identical keys, so order among them is invisible)."""
+    keys = sample(dtype, n, n % 97)
+    for desc in (False, True):
+        got = _host(g.gbs_sort_keys_msd_bitonic(_dev(keys), descending=desc))
+        assert np.array_equal(_u(got), _u(oracle.sort_keys(keys, descending=desc))), desc
+
+
+def test_msd_bitonic_hybrid_skewed_buckets(g):
+    # the AND of three draws leaves most top-16-bit prefixes near zero: buckets far above 2^14
+    # keys take the radix path, the rest the bitonic network; many buckets are empty
+    keys = wl.low_entropy_u32(1 << 20, wl.seed_for(72, 1))
+    t = _dev(keys)
+    out, temp = g.gbs_sort_keys_msd_bitonic(t, return_temp=True)
+    assert g.gbs_get_status(temp) == g.GBS_OK
+    assert np.array_equal(_host(out), oracle.sort_keys(keys))
+    g.gbs_sort_keys_msd_bitonic(t, keys_out=t, temp=temp)  # in place
+    assert np.array_equal(_host(t), oracle.sort_keys(keys))
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("seg_len", [16385, 40000, 65537])
 def test_segmented_sort_long_segments(g, dtype, seg_len):
     """Fixed-length segments above one CTA's network take the radix path, segment by segment."""
