@@ -96,15 +96,17 @@ def _wire(t: torch.Tensor) -> torch.Tensor:
 
 
 def sharded_sort(keys: torch.Tensor, vals: torch.Tensor | None = None, descending: bool = False,
-                 key_type: int | None = None, group=None, ops=None):
+                 key_type: int | None = None, group=None, ops=None, exchange_alone: bool = False):
     """Globally sorts the shards held by the ranks of `group` (every rank calls this with its own
     shard; shards may differ in size).  Returns this rank's part of the sorted keys (and the values
     that travel with them): (keys, vals).  keys: 4- or 8-byte key tensor of any gbsort key type;
-    vals: optional 4- or 8-byte values, moved with their keys (stable)."""
+    vals: optional 4- or 8-byte values, moved with their keys (stable).  A group of one rank sorts
+    locally, unless exchange_alone is set: then every step of the exchange runs with the rank as its
+    own peer (the collectives included), which checks that path on a single GPU."""
     ops = ops or DeviceOps()
     world = dist.get_world_size(group) if dist.is_initialized() else 1
     rank = dist.get_rank(group) if dist.is_initialized() else 0
-    if world == 1:
+    if world == 1 and not exchange_alone:
         return ops.sort(keys, vals, 0, 8 * keys.element_size(), descending, key_type)
 
     # 1. digit counts of every rank

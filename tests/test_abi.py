@@ -67,6 +67,13 @@ def test_temp_query_sizes(lib):
         st4, need4 = _query(lib, "gbs_sort_keys", kt, None, None, n, 0, 64, 1, None)
         assert st4 == gbsort.GBS_OK and need4 >= 8 * n
         assert _query(lib, "gbs_sort_keys", kt, None, None, n, 0, 65, 0, None)[0] == gbsort.GBS_ERR_INVALID_ARG
+    # from 2^29 keys on, the look-back status words are 64-bit: 2 KiB per tile
+    for big, per_tile in (((1 << 29) - 1, 1024), (1 << 29, 2048), (gbsort.GBS_MAX_RADIX_KEYS, 2048)):
+        st6, need6 = _query(lib, "gbs_sort_keys", gbsort.GBS_U32, None, None, big, 0, 32, 0, None)
+        tiles = (big + tile - 1) // tile
+        assert st6 == gbsort.GBS_OK
+        assert 256 + 2 * 8 * 256 * 4 + tiles * per_tile + 4 * big <= need6
+        assert need6 < 256 + 2 * 8 * 256 * 4 + tiles * per_tile + 4 * big + 4 * 256
     st3, need3 = _query(lib, "gbs_segmented_sort", gbsort.GBS_U32, None, None, 16, 1024, 0, None)
     assert st3 == gbsort.GBS_OK and need3 == 256
 

@@ -11,7 +11,9 @@ GPU test: the device steps of a multi-rank sort (digit histograms, the
 partition pass, the local sort) for several virtual ranks run one after
 another on one GPU through the C ABI, with the exchange done by slicing; the
 result is checked against the oracle.  No kernels of different ranks ever
-wait on one another."""
+wait on one another.  The exchange path itself also runs on a one-rank NCCL
+group, the rank acting as its own peer, so its collectives (histogram
+all-gather, all-to-all-v of keys and values) run through NCCL on the GPU."""
 import json
 import os
 import socket
@@ -211,3 +213,31 @@ def test_device_steps_of_a_four_rank_sort(kind, desc, pairs):
     else:
         wk = oracle.sort_keys(allin, descending=desc)
     assert np.array_equal(_u(np.concatenate(outs_k)), _u(wk))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kind,desc,pairs", [("u32", False, True), ("f64", True, False), ("u64", False, False)])
+def test_nccl_exchange_on_one_rank(kind, desc, pairs):
+    """The exchange path on a one-rank NCCL group: the all-gather of the histograms and the
+    all-to-all-v of keys and values go through NCCL with the rank as its own peer."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import torch.distributed as dist
+    from sorting_lsd_radix_gb300 import build as gbuild
+    gbuild.build()
+    keys = shard_keys(kind, 0, 300007, 3)
+    vals = np.arange(keys.size, dtype=np.uint32)
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{_free_port()}", rank=0, world_size=1)
+    try:
+        k, v = sharded.sharded_sort(torch.from_numpy(keys).cuda(),
+                                    torch.from_numpy(vals).cuda() if pairs else None,
+                                    descending=desc, exchange_alone=True)
+        torch.cuda.synchronize()
+    finally:
+        dist.destroy_process_group()
+    if pairs:
+        wk, wv = oracle.sort_pairs(keys, vals, descending=desc)
+        assert np.array_equal(v.cpu().numpy(), wv)
+    else:
+        wk = oracle.sort_keys(keys, descending=desc)
+    assert np.array_equal(_u(k.cpu().numpy()), _u(wk))
