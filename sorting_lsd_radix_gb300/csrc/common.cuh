@@ -239,27 +239,6 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
-// Thread-block clusters: the CTA's rank in its cluster, the address of a
-// shared-memory location in another CTA of the cluster, a store to such an
-// address, and a full cluster barrier (every thread of every CTA; release
-// before, acquire after).
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_map(const void *p, uint32_t cta) {
-    uint32_t a;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(cta));
-    return a;
-}
-__device__ __forceinline__ void st_cluster(uint32_t addr, uint32_t v) {
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // Records the first device-side error in the header.
 __device__ __forceinline__ void record_error(Header *h, uint32_t code, uint32_t detail) {
     if (atomicCAS(&h->error, 0u, code) == 0u) atomicExch(&h->error_detail, detail);

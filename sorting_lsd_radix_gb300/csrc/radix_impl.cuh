@@ -74,13 +74,7 @@ template <bool TRAIL = true> __device__ __forceinline__ uint32_t excl_scan_256(u
 #ifndef GBS_STORE_FULL
 #define GBS_STORE_FULL 1
 #endif
-// GBS_PAIRED: CTAs run in clusters of two on consecutive tiles 2p and 2p + 1;
-// the pair publishes one status row (the sum of both tiles' counts) and only
-// its first CTA walks the look-back, handing the second its prefix through
-// distributed shared memory.
-#ifndef GBS_PAIRED
-#define GBS_PAIRED 0
-#endif
+
 
 
 struct PeerTableLane {
@@ -305,9 +299,6 @@ template <typename K, int VB, int THREADS, int ITEMS> struct PassSmem {
     uint32_t tile;
     uint32_t num_active;  // active passes of this call
     uint32_t ordinal;     // rank of this pass among them
-    uint32_t pair;        // paired tiles: ticket of the CTA pair (tiles 2 pair and 2 pair + 1)
-    uint32_t partner_cnt[256];  // paired tiles, rank 0: the partner tile's digit counts
-    uint32_t partner_excl[256];  // paired tiles, rank 1: this tile's exclusive prefix
     alignas(8) uint64_t bar;
 };
 
@@ -678,21 +669,11 @@ __device__ __forceinline__ void pass_tile(PassSmem<K, VB, THREADS, ITEMS> &sm, c
     // ---- tile digit counts, warp offsets, publish the aggregate ------------
     uint32_t cnt = 0;
     constexpr int CB = StatusWord<SW>::COUNT_BITS;
-#if GBS_PAIRED
-    const uint32_t crank = cluster_ctarank(), row = sm.pair;  // status row: the pair
-    const bool faulty = (prm.fault_pass == prm.pass) && (prm.fault_tile >> 1 == row);
-#else
-    const uint32_t row = tile;
     const bool faulty = (prm.fault_pass == prm.pass) && (prm.fault_tile == tile);
-#endif
-    SW *my_status = reinterpret_cast<SW *>(prm.status) + (size_t)row * 256;
+    SW *my_status = reinterpret_cast<SW *>(prm.status) + (size_t)tile * 256;
     if (tid < 256) {
         cnt = tile_digit_count<WARPS>(sm.whist, tid);
-#if GBS_PAIRED
-        if (crank == 1) st_cluster(cluster_map(&sm.partner_cnt[tid], 0), cnt);
-#else
         if (!faulty) st_relaxed_gpu(my_status + tid, ((SW)(tile == 0 ? st_inc : st_agg) << CB) | cnt);
-#endif
     }
     // (wsum is not written again before the barrier after the offsets)
     const uint32_t local = excl_scan_256<false>(cnt, sm.wsum);
@@ -701,16 +682,7 @@ __device__ __forceinline__ void pass_tile(PassSmem<K, VB, THREADS, ITEMS> &sm, c
 #pragma unroll 4
         for (int w = 0; w < WARPS; ++w) sm.whist[w][tid] += local;
     }
-#if GBS_PAIRED
-    cluster_sync();  // the partner's counts have landed (and this CTA's offsets are written)
-    uint32_t pair_cnt = 0;
-    if (crank == 0 && tid < 256) {
-        pair_cnt = cnt + sm.partner_cnt[tid];
-        if (!faulty) st_relaxed_gpu(my_status + tid, ((SW)(row == 0 ? st_inc : st_agg) << CB) | pair_cnt);
-    }
-#else
     __syncthreads();
-#endif
 
     // ---- reorder the tile in shared memory by (digit, rank) ---------------
 #pragma unroll
@@ -744,24 +716,6 @@ __device__ __forceinline__ void pass_tile(PassSmem<K, VB, THREADS, ITEMS> &sm, c
     // prefix, and waits (bounded) only at a predecessor that has published
     // nothing yet.
     bool out_of_range = false;
-#if GBS_PAIRED
-    // the pair's first CTA walks back over the pairs' rows; the second gets
-    // its prefix (the first tile's prefix plus the first tile's counts)
-    uint32_t excl = 0;
-    if (crank == 0 && tid < 256) {
-        if (row > 0) {
-            excl = lookback_excl<SW>(prm, hdr, row, tid, st_agg, st_inc);
-            if (!faulty)
-                st_relaxed_gpu(my_status + tid,
-                               ((SW)st_inc << CB) | ((SW)(excl + pair_cnt) & StatusWord<SW>::COUNT_MASK));
-        }
-        st_cluster(cluster_map(&sm.partner_excl[tid], 1), excl + cnt);
-    }
-    cluster_sync();  // the prefix has landed in the second CTA
-    if (crank == 1 && tid < 256) excl = sm.partner_excl[tid];
-    if (tid < 256) {
-        sm.binoff[tid] = dbase + excl - local;
-#else
     if (tid < 256) {
         uint32_t excl = 0;
         if (tile > 0) {
@@ -770,7 +724,6 @@ __device__ __forceinline__ void pass_tile(PassSmem<K, VB, THREADS, ITEMS> &sm, c
                 st_relaxed_gpu(my_status + tid, ((SW)st_inc << CB) | ((SW)(excl + cnt) & StatusWord<SW>::COUNT_MASK));
         }
         sm.binoff[tid] = dbase + excl - local;
-#endif
         // every position of digit tid lies in [dbase + excl, dbase + excl + cnt); with counts
         // from a tile that never landed (a bounded wait gave up) they may not
         out_of_range = cnt != 0 && (uint64_t)dbase + excl + cnt > (uint64_t)prm.n;
@@ -864,7 +817,6 @@ __global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
         // Every pass is trivial: the input order is already sorted; the last
         // pass kernel copies it to the output (the in-place case needs none
         // for the keys and is finished by the copy kernel).
-        // (a launch rounded up to whole CTA pairs has a CTA past the last key)
         if (A == 0 && prm.pass == prm.num_passes - 1 && !prm.in_place && (size_t)blockIdx.x * TILE < prm.n) {
             const size_t lo = (size_t)blockIdx.x * TILE, hi = min((size_t)prm.n, lo + TILE);
             copy_range(reinterpret_cast<const K *>(prm.keys_in), reinterpret_cast<K *>(prm.keys_out), lo, hi, tid,
@@ -894,31 +846,12 @@ __global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
     // first and then that tile is copied: the tickets reach L2 in an order
     // that rarely matches the CTAs' launch order, so a copy issued before the
     // ticket returns would almost always fetch the wrong tile.
-#if GBS_PAIRED
-    // the pair's first CTA takes the pair's ticket and hands it to the second
-    const uint32_t crank = cluster_ctarank();
-    if (tid == 0) {
-        mbar_init(&sm.bar, 1);
-        fence_mbar_init();
-        if (crank == 0) {
-            const uint32_t pt = atomicAdd(&hdr->tile_counter[prm.pass], 1u);
-            sm.pair = pt;
-            st_cluster(cluster_map(&sm.pair, 1), pt);
-        }
-    }
-    cluster_sync();
-    if (tid == 0) {
-        const uint32_t t = 2 * sm.pair + crank;
-        sm.tile = t;
-        const size_t start = (size_t)t * TILE;
-#else
     if (tid == 0) {
         mbar_init(&sm.bar, 1);
         fence_mbar_init();
         const uint32_t t = atomicAdd(&hdr->tile_counter[prm.pass], 1u);
         sm.tile = t;
         const size_t start = (size_t)t * TILE;
-#endif
         if (aligned && start + TILE <= (size_t)prm.n) {
             mbar_arrive_expect_tx(&sm.bar, tx_bytes);
             bulk_g2s(sm.keys, ksrc + start, TILE * (uint32_t)sizeof(K), &sm.bar);
@@ -938,7 +871,6 @@ __global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
     __syncthreads();
     const uint32_t tile = sm.tile;
     const size_t tile_start = (size_t)tile * TILE;
-    // (a pair's second CTA past the last tile has no keys)
     const uint32_t valid = tile_start < prm.n ? (uint32_t)min((size_t)TILE, (size_t)prm.n - tile_start) : 0u;
     if (valid == TILE && aligned) {
         wait_phase(&sm.bar, 0, prm, hdr, tile);
@@ -1076,24 +1008,8 @@ template <typename K, int VB, int THREADS, int ITEMS, bool BYTE, typename SW> st
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(S));
         });
         if (e != cudaSuccess) return e;
-#if GBS_PAIRED
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((num_tiles + 1) / 2 * 2);
-        cfg.blockDim = dim3(THREADS);
-        cfg.dynamicSmemBytes = sizeof(S);
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, onesweep_pass_kernel<K, VB, THREADS, ITEMS, BYTE, SW>, prm);
-#else
         onesweep_pass_kernel<K, VB, THREADS, ITEMS, BYTE, SW><<<num_tiles, THREADS, sizeof(S), stream>>>(prm);
         return cudaGetLastError();
-#endif
     }
 };
 
