@@ -352,8 +352,8 @@ def run_gbsort(args):
 
         # The same calls with two steps in flight: step i runs on stream i % 2 with its own work
         # and output buffers, so one step's device-to-host copy overlaps the next step's
-        # host-to-device copy and sort (the host link is full duplex).  Informative; the value
-        # above is one step at a time.
+        # host-to-device copy and sort.  This throughput is the reported e2e value; the
+        # one-at-a-time figure above is kept beside it.
         streams = [torch.cuda.Stream(), torch.cuda.Stream()]
         outs = [h_out, torch.empty_like(h_in).pin_memory()]
         temps = [htemp, gbsort.gbs_sort_keys_host(h_in, outs[1], temp=None, return_temp=True,
@@ -377,8 +377,12 @@ def run_gbsort(args):
             ok = ok and gbsort.gbs_get_status(temps[j]) == gbsort.GBS_OK
             hv = outs[j].numpy()
             ok = ok and bool((hv[1:] >= hv[:-1]).all())
-        e2e["two_steps_in_flight"] = {"value": job_throughput(world, n, pms), "unit": UNIT, "ms_per_step": pms,
-                                      "streams": 2}
+        # whole-job throughput of a stream of host-buffer sorts: every step still copies its keys in
+        # and its result out through the public entry point; two are in flight on two streams
+        e2e = {"value": job_throughput(world, n, pms), "unit": UNIT, "h2d_bytes_per_step": 4 * n,
+               "d2h_bytes_per_step": 4 * n, "ms_per_step": pms, "streams": 2,
+               "api": "gbs_sort_keys_host (pinned host buffers; two steps in flight on two streams)",
+               "one_step_at_a_time": {"value": e2e["value"], "unit": UNIT, "ms_per_step": ems}}
 
     if rank != 0:
         if dist is not None:
@@ -441,9 +445,10 @@ def _active_passes(gbsort, d_keys, begin, end, desc):
     return [p for p in range(hist.shape[0]) if np.count_nonzero(hist[p]) > 1]
 
 
-def _sec_radix_keys(gen, n_default, key_type, begin=0, end=None, desc=False):
+def _sec_radix_keys(gen, n_default, key_type, begin=0, end=None, desc=False, radix_bits=8):
     def build(gbsort, torch, n=None):
         n = n or n_default
+        gbsort.gbs_debug_set_radix_bits(radix_bits)
         keys = gen(n)
         d = torch.from_numpy(keys).cuda()
         o = torch.empty_like(d)
@@ -458,8 +463,14 @@ def _sec_radix_keys(gen, n_default, key_type, begin=0, end=None, desc=False):
         alg = s * n + max(len(active), 1) * 2 * s * n
         dom = [1 + p for p in active] if active else [passes]
         call = lambda: gbsort.gbs_sort_keys(d, o, begin_bit=begin, end_bit=end, descending=desc, temp=temp)
-        return call, temp, n, alg, 2 * s * n, dom, {"active_passes": len(active),
-                                                    "oracle_sample": (keys, begin, stop, desc)}
+        extra = {"active_passes": len(active), "oracle_sample": (keys, begin, stop, desc)}
+        if radix_bits != 8:
+            # 11-bit digits: ceil(bits / 11) passes; all of them active on these workloads
+            passes = (stop - begin + radix_bits - 1) // radix_bits
+            alg = s * n + passes * 2 * s * n
+            dom = list(range(1, passes + 1))
+            extra.update({"active_passes": passes, "radix_bits": radix_bits})
+        return call, temp, n, alg, 2 * s * n, dom, extra
     return build
 
 
@@ -556,6 +567,14 @@ SECONDARY = {
                           _sec_radix_keys(lambda n: wl.all_equal_u32(n, wl.seed_for(3, 1)), N_KEYS, "u32")),
     "u32_1e8_msd_bitonic": ("sort_keys u32 n=1e8 uniform by the hybrid prototype: MSD radix over the top 16 bits, "
                             "then a bitonic sort of each of the 65536 buckets", _sec_msd_bitonic(N_KEYS)),
+    "u32_1e8_radix11": ("sort_keys u32 n=1e8 uniform with the 11-bit-digit prototype (3 passes)",
+                        _sec_radix_keys(lambda n: wl.uniform_u32(n, SEED), N_KEYS, "u32", radix_bits=11)),
+    "i64_2p27_radix11": ("sort_keys i64 n=2^27 uniform with the 11-bit-digit prototype (6 passes)",
+                         _sec_radix_keys(lambda n: wl.uniform_i64(n, wl.seed_for(6, 1)), 1 << 27, "i64",
+                                         radix_bits=11)),
+    "f64_2p27_radix11": ("sort_keys f64 n=2^27 N(0,1000) with signed zeros and infinities, 11-bit-digit prototype",
+                         _sec_radix_keys(lambda n: wl.normal_mix_f64(n, wl.seed_for(6, 0)), 1 << 27, "f64",
+                                         radix_bits=11)),
     "u32_1e8_bits0_16": ("sort_keys u32 n=1e8 uniform, bits [0,16)",
                          _sec_radix_keys(lambda n: wl.uniform_u32(n, SEED), N_KEYS, "u32", 0, 16)),
     "f32_2p28": ("sort_keys f32 n=2^28, N(0,1000) with signed zeros and infinities",

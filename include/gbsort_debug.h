@@ -35,6 +35,15 @@ void gbs_debug_set_lookback_fault(int pass, uint32_t tile, uint32_t spin_limit);
  */
 void gbs_debug_set_timing_events(void **events, int count);
 
+/*
+ * Digit width of the radix sort's later keys-only calls with fewer than 2^29
+ * keys: 8 (the library's path, the default) or 11, a measured prototype with
+ * 2048 digit values per pass (3 passes for 32-bit keys, 6 for 64-bit keys
+ * instead of 4 and 8).  Same results; pairs and larger sorts keep 8-bit
+ * digits.  Any other value restores 8.  Process-wide; not thread-safe.
+ */
+void gbs_debug_set_radix_bits(int bits);
+
 /* Number of kernels the calling thread's last sorting call launched. */
 int gbs_debug_last_launch_count(void);
 

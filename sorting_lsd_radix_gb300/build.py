@@ -14,7 +14,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgbsort.so")
-SOURCES = ["api.cu", "radix.cu", "radix_wide.cu", "bitonic.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "radix.cu", "radix_wide.cu", "radix11.cu", "bitonic.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

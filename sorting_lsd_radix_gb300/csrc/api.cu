@@ -33,6 +33,7 @@ int key_bytes_of(gbs_key_type kt) {
 int g_fault_pass = -1;
 uint32_t g_fault_tile = 0;
 uint32_t g_spin_limit = DEFAULT_SPIN_LIMIT;
+int g_radix_bits = 8;  // 11: keys-only sorts of fewer than 2^29 keys take the 11-bit-digit prototype
 thread_local int t_launches = 0;
 thread_local void **t_events = nullptr;
 thread_local int t_event_count = 0;
@@ -52,17 +53,22 @@ struct Layout {
     uint32_t num_tiles;
 };
 
+// The 11-bit-digit prototype serves this call (test hook; keys only, < 2^29 keys).
+bool use_radix11(int val_bytes, size_t n) { return g_radix_bits == 11 && val_bytes == 0 && n < gbs::WIDE_STATUS_MIN_KEYS; }
+
 Layout radix_layout(int key_bytes, int val_bytes, size_t n) {
     Layout l;
-    const uint32_t tile = gbs::radix_tile_keys(key_bytes, val_bytes);
+    const bool r11 = use_radix11(val_bytes, n);
+    const uint32_t tile = r11 ? gbs::radix11_tile_keys(key_bytes) : gbs::radix_tile_keys(key_bytes, val_bytes);
+    const size_t digits = r11 ? 2048 : 256;  // histogram and status words per digit position / tile
     l.num_tiles = (uint32_t)((n + tile - 1) / tile);
     size_t off = sizeof(Header);
     l.hist = off;
-    off += round_up(sizeof(uint32_t) * gbs::MAX_PASSES * 256);
+    off += round_up(sizeof(uint32_t) * gbs::MAX_PASSES * digits);
     l.digit_base = off;
-    off += round_up(sizeof(uint32_t) * gbs::MAX_PASSES * 256);
+    off += round_up(sizeof(uint32_t) * gbs::MAX_PASSES * digits);
     l.status = off;
-    off += round_up(gbs::status_bytes(n, l.num_tiles));
+    off += round_up(r11 ? sizeof(uint32_t) * digits * l.num_tiles : gbs::status_bytes(n, l.num_tiles));
     l.keys_alt = off;
     off += round_up((size_t)key_bytes * n);
     l.vals_alt = off;
@@ -117,7 +123,8 @@ gbs_status radix_common(void *d_temp, size_t *temp_bytes, gbs_key_type kt, const
     cudaError_t e = cudaMemsetAsync(tb + keep, 0, lay.digit_base - keep, s);  // header + histograms
     if (e != cudaSuccess) return GBS_ERR_CUDA;
 
-    const int passes = (end_bit - begin_bit + 7) / 8;
+    const bool r11 = use_radix11(val_bytes, n);
+    const int passes = r11 ? (end_bit - begin_bit + 10) / 11 : (end_bit - begin_bit + 7) / 8;
     if (n <= 1 || passes == 0) {
         e = copy_if_needed(keys_in, keys_out, n * kb, s);
         if (e == cudaSuccess && pairs) e = copy_if_needed(vals_in, vals_out, n * (size_t)val_bytes, s);
@@ -155,6 +162,7 @@ gbs_status radix_common(void *d_temp, size_t *temp_bytes, gbs_key_type kt, const
     job.spin_limit = g_spin_limit;
     job.fault_pass = g_fault_pass;
     job.fault_tile = g_fault_tile;
+    if (r11) return from_cuda(gbs::launch_radix11_sort(job, s, &t_launches));
     return from_cuda(gbs::launch_radix_sort(job, s, &t_launches));
 }
 
@@ -486,6 +494,8 @@ void gbs_debug_set_timing_events(void **events, int count) {
     t_events = events;
     t_event_count = events ? count : 0;
 }
+
+void gbs_debug_set_radix_bits(int bits) { g_radix_bits = bits == 11 ? 11 : 8; }
 
 size_t gbs_debug_radix_tile_keys(int key_bytes, int value_bytes) {
     return gbs::radix_tile_keys(key_bytes, value_bytes == 8 ? 8 : value_bytes ? 4 : 0);

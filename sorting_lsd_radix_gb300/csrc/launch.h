@@ -83,6 +83,11 @@ void timing_mark(cudaStream_t stream);
 // value width (0: keys only).
 uint32_t radix_tile_keys(int key_bytes, int val_bytes);
 
+// The 11-bit-digit prototype (radix11.cu): keys only, fewer than 2^29 keys;
+// hist / digit_base hold [passes][2048] words and status [tiles][2048] words.
+uint32_t radix11_tile_keys(int key_bytes);
+cudaError_t launch_radix11_sort(const RadixJob &job, cudaStream_t stream, int *launches);
+
 // The digit passes of a job with 64-bit look-back status words (radix_wide.cu).
 cudaError_t launch_passes_wide(const RadixJob &job, cudaStream_t stream, int *launches);
 

@@ -40,7 +40,7 @@ EXPORTS = ("gbs_sort_keys", "gbs_sort_pairs", "gbs_segmented_sort", "gbs_digit_h
            "gbs_status_string", "gbs_version", "gbs_debug_set_lookback_fault", "gbs_debug_last_launch_count",
            "gbs_debug_radix_tile_keys", "gbs_debug_set_timing_events", "gbs_sort_keys_noalloc",
            "gbs_sort_keys_host", "gbs_segmented_sort_offsets", "gbs_sort_pairs64", "gbs_get_status_noalloc",
-           "gbs_sort_keys_msd_bitonic")
+           "gbs_sort_keys_msd_bitonic", "gbs_debug_set_radix_bits")
 GBS_NOALLOC_MAX_KEYS = 1 << 20
 
 
@@ -82,6 +82,8 @@ def load(path: str | None = None):
     lib.gbs_sort_keys_noalloc.restype = i
     lib.gbs_sort_keys_msd_bitonic.argtypes = [vp, szp, i, vp, vp, sz, i, vp]
     lib.gbs_sort_keys_msd_bitonic.restype = i
+    lib.gbs_debug_set_radix_bits.argtypes = [i]
+    lib.gbs_debug_set_radix_bits.restype = None
     lib.gbs_get_status_noalloc.argtypes = [vp]
     lib.gbs_get_status_noalloc.restype = i
     lib.gbs_get_status.argtypes = [vp, sz, vp]
@@ -351,6 +353,11 @@ def gbs_get_status(temp: torch.Tensor, stream=None) -> int:
 
 def gbs_debug_set_lookback_fault(pass_index: int, tile: int, spin_limit: int) -> None:
     load().gbs_debug_set_lookback_fault(pass_index, tile, spin_limit)
+
+
+def gbs_debug_set_radix_bits(bits: int) -> None:
+    """8 (default) or 11: digit width of later keys-only radix sorts below 2^29 keys (test hook)."""
+    load().gbs_debug_set_radix_bits(bits)
 
 
 def gbs_debug_last_launch_count() -> int:

@@ -324,6 +324,31 @@ SEG_MIX = [0, 1, 2, 3, 5, 17, 100, 255, 256, 1000, 1023, 1024, 1025, 2047, 4097,
            20000, 70001, 0, 7, 300, 3000]
 
 
+R11_SIZES = [16385, 4095 * 5, 4096 * 7, 8192 * 3 + 1, 8192 * 5, 100003, (1 << 20) + 9]
+R11_RANGES = {np.uint32: [(0, 32), (0, 22), (5, 27), (21, 32)], np.int32: [(0, 32)], np.float32: [(0, 32), (9, 31)],
+              np.uint64: [(0, 64), (0, 33), (40, 64)], np.int64: [(0, 64)], np.float64: [(0, 64), (11, 55)]}
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("n", R11_SIZES)
+def test_radix11_prototype(g, dtype, n):
+    """The 11-bit-digit prototype (2048 digit values per pass) sorts exactly like the 8-bit path:
+    every key type, both orders, partial bit ranges, ties, in place."""
+    keys = sample(dtype, n, n % 89) if n % 2 else with_ties(dtype, n, n % 89)
+    g.gbs_debug_set_radix_bits(11)
+    try:
+        for b, e in R11_RANGES[dtype]:
+            for desc in (False, True):
+                out, temp = g.gbs_sort_keys(_dev(keys), begin_bit=b, end_bit=e, descending=desc, return_temp=True)
+                assert g.gbs_get_status(temp) == g.GBS_OK
+                assert np.array_equal(_u(_host(out)), _u(oracle.sort_keys(keys, b, e, descending=desc))), (b, e, desc)
+        t = _dev(keys)
+        g.gbs_sort_keys(t, keys_out=t)  # in place (an odd number of passes for 32-bit keys)
+        assert np.array_equal(_u(_host(t)), _u(oracle.sort_keys(keys)))
+    finally:
+        g.gbs_debug_set_radix_bits(8)
+
+
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("n", [16385, 100003, 1 << 21])
 def test_msd_bitonic_hybrid(g, dtype, n):
