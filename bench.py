@@ -111,7 +111,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
 
@@ -142,6 +142,16 @@ class ClockSampler:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def max_sm_clock_hz(gpu_index=0):
+    """The GPU's maximum SM clock from nvidia-smi; 2070 MHz (GB300) if it cannot be read."""
+    try:
+        out = subprocess.run(["nvidia-smi", "-i", str(gpu_index), "--query-gpu=clocks.max.sm",
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=10).stdout
+        return float(out.strip().splitlines()[0]) * 1e6
+    except Exception:
+        return 2070e6
 
 
 def dist_setup(args):
@@ -668,6 +678,19 @@ def run_secondary(args):
             "kernel_ms": per_kernel.tolist(), "launches": launches}
     if "comparators_per_call" in extra:
         line["comparators_per_s"] = extra["comparators_per_call"] / (ms / 1e3)
+        # ALU roofline of the bitonic network: a compare-exchange is a min, a max and the
+        # direction's complement (3 logic-pipe ops per pair of keys); the logic pipe retires 2 warp
+        # instructions per clock per SM (64 lane ops)
+        props = torch.cuda.get_device_properties(0)
+        sm_clock_hz = max_sm_clock_hz()
+        alu_peak = props.multi_processor_count * 64 * sm_clock_hz / 3
+        kernel_ms = float(per_kernel.sum()) if launches else ms
+        line["alu_roofline"] = {"bound": "alu", "achieved": extra["comparators_per_call"] / (kernel_ms / 1e3),
+                                "peak": alu_peak, "unit": "compare-exchanges/s",
+                                "frac": extra["comparators_per_call"] / (kernel_ms / 1e3) / alu_peak,
+                                "peak_basis": f"{props.multi_processor_count} SMs x 64 logic-pipe lane ops per clock "
+                                              f"x {sm_clock_hz / 1e9:.2f} GHz (maximum SM clock) / 3 ops per "
+                                              f"compare-exchange"}
     sample = extra.pop("oracle_sample", None)
     line.update({k: v for k, v in extra.items() if k != "comparators_per_call"})
     if temp is not None:

@@ -241,3 +241,18 @@ def test_nccl_exchange_on_one_rank(kind, desc, pairs):
     else:
         wk = oracle.sort_keys(keys, descending=desc)
     assert np.array_equal(_u(k.cpu().numpy()), _u(wk))
+
+
+@pytest.mark.gpu
+def test_sharded_segmented_sort_blocks():
+    """Segments shard with no collective: each rank sorts its own consecutive block of segments.
+    Without a process group the one rank's block is every segment."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sorting_lsd_radix_gb300 import build as gbuild
+    gbuild.build()
+    segs, seg_len = 37, 3000
+    keys = shard_keys("u32", 0, segs * seg_len, 5)
+    out, first = sharded.sharded_segmented_sort(torch.from_numpy(keys).cuda(), segs, seg_len, descending=True)
+    assert first == 0 and out.numel() == keys.size
+    assert np.array_equal(out.cpu().numpy(), oracle.segmented_sort(keys, segs, seg_len, descending=True))
