@@ -118,7 +118,7 @@ struct alignas(256) Header {
     uint32_t num_active;        // passes whose digit is not constant
     uint32_t active_mask;       // bit p set: pass p runs
     uint32_t ordinal[MAX_PASSES];       // rank of pass p among active passes
-    uint32_t tile_counter[MAX_PASSES];  // dynamic tile tickets of pass p
+    uint32_t tile_counter[MAX_PASSES];  // tile tickets of pass p (11-bit prototype; the 8-bit passes use block indices)
 };
 static_assert(sizeof(Header) == 256, "header must be 256 bytes");
 

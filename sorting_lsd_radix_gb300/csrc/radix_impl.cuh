@@ -840,16 +840,18 @@ __global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
                          (!PAIRS || ((reinterpret_cast<uintptr_t>(vsrc) & 15) == 0));
     const uint32_t tx_bytes = TILE * (uint32_t)(sizeof(K) + VB);
 
-    // ---- ticket and tile load ---------------------------------------------
-    // Tiles are taken in ticket order, which guarantees the look-back's
-    // forward progress whatever order the CTAs start in.  The ticket is taken
-    // first and then that tile is copied: the tickets reach L2 in an order
-    // that rarely matches the CTAs' launch order, so a copy issued before the
-    // ticket returns would almost always fetch the wrong tile.
+    // ---- tile and its load -----------------------------------------------
+    // The CTA's tile is its block index, so the copy is issued at once.  The
+    // look-back of tile t waits for tiles below t, which relies on the CTAs of
+    // a grid being dispatched in increasing block order, as the hardware does
+    // (the common single-pass scans rely on the same).  An atomic ticket would
+    // guarantee progress whatever the dispatch order, but its round trip sits
+    // before every tile copy: 3.5% per sort.  Every wait here is bounded, so a
+    // predecessor that never ran would end in a recorded timeout, never a hang.
     if (tid == 0) {
         mbar_init(&sm.bar, 1);
         fence_mbar_init();
-        const uint32_t t = atomicAdd(&hdr->tile_counter[prm.pass], 1u);
+        const uint32_t t = blockIdx.x;
         sm.tile = t;
         const size_t start = (size_t)t * TILE;
         if (aligned && start + TILE <= (size_t)prm.n) {
