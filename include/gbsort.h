@@ -121,6 +121,40 @@ gbs_status gbs_sort_keys_host(void *d_temp, size_t *temp_bytes, gbs_key_type key
                               void *h_keys_out, size_t n, int begin_bit, int end_bit, int descending, void *stream);
 
 /*
+ * gbs_sort_keys_host_batch — gbs_sort_keys_host on `count` independent host
+ * arrays (same key type, bit range and order for all), with the transfers of
+ * neighbouring arrays overlapped: while array i is sorted on `stream`, array
+ * i + 1 is copied to the device and array i - 1 copied back, on two streams
+ * of the library's own (created for the call with their events and released
+ * when it returns; no memory is allocated).  The two directions of the host
+ * link then run at the same time.  Each array's result equals
+ * gbs_sort_keys_host's.
+ *   h_keys_in[i], h_keys_out[i]  host arrays of n[i] keys.  h_keys_out[i]
+ *               may equal h_keys_in[i] (in place) but must not overlap any
+ *               other entry's input; inputs may repeat, and so may outputs
+ *               (the copies back run in batch order: a repeated output ends
+ *               holding the result of its last entry)
+ *   n           host array of the count sizes, each at most GBS_MAX_RADIX_KEYS
+ *   count       number of arrays (0: only the status header is cleared)
+ *   d_temp      device work buffer (query with d_temp == NULL): one sort work
+ *               buffer for the largest n[i], then three device key buffers of
+ *               that size (an array's buffer is reused by array i + 3 once its
+ *               copy back has finished)
+ * The sorts run one after another on `stream`; the copies start after the
+ * work enqueued on `stream` before the call, and everything the call enqueues
+ * has finished when `stream` reaches the call's end, so the caller
+ * synchronises `stream` alone.  Page-locked host buffers are needed for the
+ * overlap.  gbs_get_status(d_temp, ...) reports the first device-side error
+ * of any sort in the batch.  Errors: GBS_ERR_INVALID_ARG (a NULL array with
+ * count > 0, a NULL pointer for an array with n[i] > 0, a bad bit range),
+ * GBS_ERR_UNSUPPORTED (an n[i] above GBS_MAX_RADIX_KEYS), GBS_ERR_CUDA (a
+ * failed enqueue: the work enqueued before it still joins `stream`).
+ */
+gbs_status gbs_sort_keys_host_batch(void *d_temp, size_t *temp_bytes, gbs_key_type key_type,
+                                    const void *const *h_keys_in, void *const *h_keys_out, const size_t *n,
+                                    size_t count, int begin_bit, int end_bit, int descending, void *stream);
+
+/*
  * gbs_sort_pairs — like gbs_sort_keys, moving one uint32_t value with each
  * key.  Stable: pairs with equal codes keep their input order.
  *   d_vals_in / d_vals_out  device arrays of n uint32_t; may be equal

@@ -187,6 +187,38 @@ static_assert((int)GBS_U32 == gbs::KIND_U32 && (int)GBS_I32 == gbs::KIND_I32 && 
                   (int)GBS_U64 == gbs::KIND_U64 && (int)GBS_I64 == gbs::KIND_I64 && (int)GBS_F64 == gbs::KIND_F64,
               "the ABI's key types are the kernels' key kinds");
 
+namespace {
+// Streams and events of one batch call, released when the call returns (work
+// still pending on them completes first: the runtime defers the release).
+struct BatchStreams {
+    static constexpr int SLOTS = 3;
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, in_done[SLOTS] = {}, sorted[SLOTS] = {}, out_done[SLOTS] = {};
+    cudaEvent_t in_end = nullptr, out_end = nullptr;
+    cudaError_t create() {
+        cudaError_t e = cudaStreamCreateWithFlags(&in, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&out, cudaStreamNonBlocking);
+        cudaEvent_t *all[] = {&start, &in_end, &out_end};
+        for (cudaEvent_t *ev : all)
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+        for (int j = 0; j < SLOTS && e == cudaSuccess; ++j) {
+            e = cudaEventCreateWithFlags(&in_done[j], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sorted[j], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&out_done[j], cudaEventDisableTiming);
+        }
+        return e;
+    }
+    ~BatchStreams() {
+        cudaEvent_t evs[] = {start, in_end, out_end, in_done[0], in_done[1], in_done[2], sorted[0], sorted[1],
+                             sorted[2], out_done[0], out_done[1], out_done[2]};
+        for (cudaEvent_t ev : evs)
+            if (ev) cudaEventDestroy(ev);
+        if (in) cudaStreamDestroy(in);
+        if (out) cudaStreamDestroy(out);
+    }
+};
+}  // namespace
+
 extern "C" {
 
 gbs_status gbs_sort_keys(void *d_temp, size_t *temp_bytes, gbs_key_type key_type, const void *d_keys_in,
@@ -221,6 +253,78 @@ gbs_status gbs_sort_keys_host(void *d_temp, size_t *temp_bytes, gbs_key_type key
                       descending, stream);
     if (st != GBS_OK || n == 0) return st;
     return from_cuda(cudaMemcpyAsync(h_keys_out, d_keys, n * kb, cudaMemcpyDeviceToHost, s));
+}
+
+
+gbs_status gbs_sort_keys_host_batch(void *d_temp, size_t *temp_bytes, gbs_key_type key_type,
+                                    const void *const *h_keys_in, void *const *h_keys_out, const size_t *n,
+                                    size_t count, int begin_bit, int end_bit, int descending, void *stream) {
+    constexpr int SLOTS = BatchStreams::SLOTS;
+    const int kb = key_bytes_of(key_type);
+    if (kb == 0 || temp_bytes == nullptr) return GBS_ERR_INVALID_ARG;
+    if (begin_bit < 0 || end_bit < begin_bit || end_bit > 8 * kb) return GBS_ERR_INVALID_ARG;
+    if (count > 0 && (n == nullptr || h_keys_in == nullptr || h_keys_out == nullptr)) return GBS_ERR_INVALID_ARG;
+    size_t max_n = 0;
+    for (size_t i = 0; i < count; ++i) {
+        if (n[i] > GBS_MAX_RADIX_KEYS) return GBS_ERR_UNSUPPORTED;
+        max_n = std::max(max_n, n[i]);
+    }
+    // work buffer: one sort work buffer for the largest array (a smaller
+    // array's layout fits inside it), then SLOTS device key buffers
+    size_t sort_bytes = 0;
+    gbs_status st = radix_common(nullptr, &sort_bytes, key_type, nullptr, nullptr, nullptr, nullptr, 0, max_n,
+                                 begin_bit, end_bit, descending, stream);
+    if (st != GBS_OK) return st;
+    const size_t keys_off = round_up(sort_bytes), slot_bytes = round_up((size_t)kb * max_n);
+    bool query = false;
+    st = check_temp(d_temp, temp_bytes, keys_off + SLOTS * slot_bytes, &query);
+    if (st != GBS_OK || query) return st;
+    for (size_t i = 0; i < count; ++i)
+        if (n[i] > 0 && (h_keys_in[i] == nullptr || h_keys_out[i] == nullptr)) return GBS_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    size_t inner = keys_off;
+    if (count == 0)  // clears the status header, as a sort of no keys does
+        return radix_common(d_temp, &inner, key_type, nullptr, nullptr, nullptr, nullptr, 0, 0, begin_bit, end_bit,
+                            descending, stream);
+
+    BatchStreams bs;
+    if (bs.create() != cudaSuccess) return GBS_ERR_CUDA;
+    // the copies follow the work enqueued on `stream` before the call
+    cudaError_t e = cudaEventRecord(bs.start, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(bs.in, bs.start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(bs.out, bs.start, 0);
+    if (e != cudaSuccess) return GBS_ERR_CUDA;
+    unsigned char *slots = reinterpret_cast<unsigned char *>(d_temp) + keys_off;
+    for (size_t i = 0; i < count && st == GBS_OK; ++i) {
+        const int j = (int)(i % SLOTS);
+        void *d_keys = slots + j * slot_bytes;
+        const size_t bytes = n[i] * kb;
+        // array i - SLOTS used this buffer: its copy back must have finished
+        if (i >= (size_t)SLOTS) e = cudaStreamWaitEvent(bs.in, bs.out_done[j], 0);
+        if (e == cudaSuccess && bytes) e = cudaMemcpyAsync(d_keys, h_keys_in[i], bytes, cudaMemcpyHostToDevice, bs.in);
+        if (e == cudaSuccess) e = cudaEventRecord(bs.in_done[j], bs.in);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, bs.in_done[j], 0);
+        if (e != cudaSuccess) {
+            st = GBS_ERR_CUDA;
+            break;
+        }
+        // the first sort clears the header's error word, the others keep it
+        st = radix_common(d_temp, &inner, key_type, d_keys, d_keys, nullptr, nullptr, 0, n[i], begin_bit, end_bit,
+                          descending, stream, i > 0);
+        if (st != GBS_OK) break;
+        e = cudaEventRecord(bs.sorted[j], s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(bs.out, bs.sorted[j], 0);
+        if (e == cudaSuccess && bytes) e = cudaMemcpyAsync(h_keys_out[i], d_keys, bytes, cudaMemcpyDeviceToHost, bs.out);
+        if (e == cudaSuccess) e = cudaEventRecord(bs.out_done[j], bs.out);
+        if (e != cudaSuccess) st = GBS_ERR_CUDA;
+    }
+    // join: `stream` passes the call's end only after both side streams' work
+    e = cudaEventRecord(bs.in_end, bs.in);
+    if (e == cudaSuccess) e = cudaEventRecord(bs.out_end, bs.out);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, bs.in_end, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, bs.out_end, 0);
+    if (st == GBS_OK && e != cudaSuccess) st = GBS_ERR_CUDA;
+    return st;
 }
 
 gbs_status gbs_sort_pairs(void *d_temp, size_t *temp_bytes, gbs_key_type key_type, const void *d_keys_in,

@@ -40,7 +40,7 @@ EXPORTS = ("gbs_sort_keys", "gbs_sort_pairs", "gbs_segmented_sort", "gbs_digit_h
            "gbs_status_string", "gbs_version", "gbs_debug_set_lookback_fault", "gbs_debug_last_launch_count",
            "gbs_debug_radix_tile_keys", "gbs_debug_set_timing_events", "gbs_sort_keys_noalloc",
            "gbs_sort_keys_host", "gbs_segmented_sort_offsets", "gbs_sort_pairs64", "gbs_get_status_noalloc",
-           "gbs_sort_keys_msd_bitonic", "gbs_debug_set_radix_bits")
+           "gbs_sort_keys_msd_bitonic", "gbs_debug_set_radix_bits", "gbs_sort_keys_host_batch")
 GBS_NOALLOC_MAX_KEYS = 1 << 20
 
 
@@ -67,6 +67,9 @@ def load(path: str | None = None):
     lib.gbs_sort_keys.argtypes = [vp, szp, i, vp, vp, sz, i, i, i, vp]
     lib.gbs_sort_keys.restype = i
     lib.gbs_sort_keys_host.argtypes = [vp, szp, i, vp, vp, sz, i, i, i, vp]
+    lib.gbs_sort_keys_host_batch.restype = i
+    lib.gbs_sort_keys_host_batch.argtypes = [vp, szp, i, ctypes.POINTER(vp), ctypes.POINTER(vp), szp, sz, i, i, i,
+                                             vp]
     lib.gbs_sort_keys_host.restype = i
     lib.gbs_sort_pairs.argtypes = [vp, szp, i, vp, vp, vp, vp, sz, i, i, i, vp]
     lib.gbs_sort_pairs64.argtypes = [vp, szp, i, vp, vp, vp, vp, sz, i, i, i, vp]
@@ -230,6 +233,35 @@ def gbs_sort_keys_host(keys_in: torch.Tensor, keys_out: torch.Tensor | None = No
         end_bit = 8 * _KIND_BYTES[kind]
     args = (kind, _ptr(keys_in), _ptr(keys_out), n, begin_bit, end_bit, int(bool(descending)), _stream(stream))
     temp = _run(load().gbs_sort_keys_host, args, temp, "gbs_sort_keys_host")
+    return (keys_out, temp) if return_temp else keys_out
+
+
+def gbs_sort_keys_host_batch(keys_in: list, keys_out: list | None = None, begin_bit: int = 0,
+                             end_bit: int | None = None, descending: bool = False, temp: torch.Tensor | None = None,
+                             key_type: int | None = None, stream=None, return_temp: bool = False):
+    """gbs_sort_keys_host on a list of CPU tensors of one dtype, with the copies of neighbouring arrays
+    overlapped (see the C entry point).  keys_out: a list of CPU tensors of the same sizes (an entry may be
+    the matching keys_in), or None to allocate them (page-locked when the inputs are).  Asynchronous on the
+    stream: synchronise it before reading the outputs."""
+    kind = _kind(keys_in[0], key_type) if keys_in else (GBS_U32 if key_type is None else key_type)
+    for t in keys_in:
+        if t.is_cuda or not t.is_contiguous() or t.dtype != keys_in[0].dtype:
+            raise ValueError("keys_in must be contiguous CPU tensors of one dtype")
+    if keys_out is None:
+        keys_out = [torch.empty_like(t, pin_memory=t.is_pinned()) for t in keys_in]
+    if len(keys_out) != len(keys_in):
+        raise ValueError("keys_out must hold one tensor per input")
+    for t, o in zip(keys_in, keys_out):
+        if o.is_cuda or not o.is_contiguous() or o.numel() != t.numel() or o.dtype != t.dtype:
+            raise ValueError("each keys_out entry must be a contiguous CPU tensor like its input")
+    if end_bit is None:
+        end_bit = 8 * _KIND_BYTES[kind]
+    count = len(keys_in)
+    ins = (ctypes.c_void_p * max(count, 1))(*[_ptr(t) for t in keys_in])
+    outs = (ctypes.c_void_p * max(count, 1))(*[_ptr(t) for t in keys_out])
+    ns = (ctypes.c_size_t * max(count, 1))(*[t.numel() for t in keys_in])
+    args = (kind, ins, outs, ns, count, begin_bit, end_bit, int(bool(descending)), _stream(stream))
+    temp = _run(load().gbs_sort_keys_host_batch, args, temp, "gbs_sort_keys_host_batch")
     return (keys_out, temp) if return_temp else keys_out
 
 

@@ -103,6 +103,56 @@ def test_host_entry_rejects_bad_arguments(lib):
         gbsort.GBS_ERR_INVALID_ARG
 
 
+def _batch_args(sizes, ins=None, outs=None):
+    k = max(len(sizes), 1)
+    fake = 1 << 40  # never dereferenced: the checks fail first
+    ins = (ctypes.c_void_p * k)(*(ins if ins is not None else [fake] * len(sizes)))
+    outs = (ctypes.c_void_p * k)(*(outs if outs is not None else [fake] * len(sizes)))
+    ns = (ctypes.c_size_t * k)(*sizes)
+    return ins, outs, ns
+
+
+def test_host_batch_temp_holds_one_sort_buffer_and_three_key_buffers(lib):
+    sizes = [10**6, 7, 3 * 10**6 + 5, 0]
+    ins, outs, ns = _batch_args(sizes)
+    _, sort_need = _query(lib, "gbs_sort_keys", gbsort.GBS_U32, None, None, max(sizes), 0, 32, 0, None)
+    st, need = _query(lib, "gbs_sort_keys_host_batch", gbsort.GBS_U32, ins, outs, ns, len(sizes), 0, 32, 0, None)
+    assert st == gbsort.GBS_OK
+    slot = (4 * max(sizes) + 255) // 256 * 256
+    assert need - 3 * slot in range(sort_need, sort_need + 256)
+    # 64-bit keys: the slots hold 8 bytes per key
+    _, sort64 = _query(lib, "gbs_sort_keys", gbsort.GBS_F64, None, None, max(sizes), 0, 64, 1, None)
+    st, need64 = _query(lib, "gbs_sort_keys_host_batch", gbsort.GBS_F64, ins, outs, ns, len(sizes), 0, 64, 1, None)
+    assert st == gbsort.GBS_OK and need64 - 3 * ((8 * max(sizes) + 255) // 256 * 256) in range(sort64, sort64 + 256)
+    # an empty batch needs the header of a sort of no keys
+    st, need0 = _query(lib, "gbs_sort_keys_host_batch", gbsort.GBS_U32, None, None, None, 0, 0, 32, 0, None)
+    assert st == gbsort.GBS_OK and need0 == _query(lib, "gbs_sort_keys", gbsort.GBS_U32, None, None, 0, 0, 32, 0,
+                                                   None)[1]
+
+
+def test_host_batch_rejects_bad_arguments(lib):
+    ins, outs, ns = _batch_args([1000, 2000])
+    q = lambda *a: _query(lib, "gbs_sort_keys_host_batch", *a)[0]
+    assert q(9, ins, outs, ns, 2, 0, 8, 0, None) == gbsort.GBS_ERR_INVALID_ARG
+    assert q(gbsort.GBS_I32, ins, outs, ns, 2, 4, 40, 0, None) == gbsort.GBS_ERR_INVALID_ARG
+    assert q(gbsort.GBS_U32, ins, outs, None, 2, 0, 32, 0, None) == gbsort.GBS_ERR_INVALID_ARG
+    assert q(gbsort.GBS_U32, None, outs, ns, 2, 0, 32, 0, None) == gbsort.GBS_ERR_INVALID_ARG
+    assert q(gbsort.GBS_U32, ins, None, ns, 2, 0, 32, 0, None) == gbsort.GBS_ERR_INVALID_ARG
+    big = _batch_args([10, gbsort.GBS_MAX_RADIX_KEYS + 1])
+    assert q(gbsort.GBS_U32, *big, 2, 0, 32, 0, None) == gbsort.GBS_ERR_UNSUPPORTED
+    fake = ctypes.c_void_p(1 << 40)
+    small = ctypes.c_size_t(1000)
+    assert lib.gbs_sort_keys_host_batch(fake, ctypes.byref(small), gbsort.GBS_U32, ins, outs, ns, 2, 0, 32, 0,
+                                        None) == gbsort.GBS_ERR_TEMP_TOO_SMALL
+    roomy = ctypes.c_size_t(1 << 30)
+    nul = _batch_args([1000, 2000], ins=[1 << 40, 0])
+    assert lib.gbs_sort_keys_host_batch(fake, ctypes.byref(roomy), gbsort.GBS_U32, *nul, 2, 0, 32, 0,
+                                        None) == gbsort.GBS_ERR_INVALID_ARG
+    unaligned = ctypes.c_void_p((1 << 40) + 8)
+    assert lib.gbs_sort_keys_host_batch(unaligned, ctypes.byref(roomy), gbsort.GBS_U32, ins, outs, ns, 2, 0, 32, 0,
+                                        None) == gbsort.GBS_ERR_INVALID_ARG
+
+
 def _offsets(values):
     a = (ctypes.c_uint64 * len(values))(*values)
     return a

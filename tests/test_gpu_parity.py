@@ -210,6 +210,56 @@ def test_sort_keys_host_in_place_bit_ranges(g, bits):
     assert np.array_equal(h.numpy(), oracle.sort_keys(keys, bits[0], bits[1]))
 
 
+BATCH_SIZES = [5000, 0, 2 * TILE32 + 13, 1, 16385, 3, 100003, 16384, 2 * TILE32 + 13]
+
+
+@pytest.mark.parametrize("dtype", [np.uint32, np.float32, np.int64, np.float64])
+@pytest.mark.parametrize("descending", [False, True])
+def test_sort_keys_host_batch(g, dtype, descending):
+    """Arrays of mixed sizes (empty, one key, the one-CTA bitonic path, several ragged radix tiles) sorted
+    by one batch call; more arrays than device key buffers, so buffers are reused; one array in place."""
+    keys = [sample(dtype, n, 300 + i) if i % 3 else with_ties(dtype, n, 300 + i) for i, n in enumerate(BATCH_SIZES)]
+    h_in = [torch.from_numpy(np.ascontiguousarray(k)).pin_memory() for k in keys]
+    h_out = [torch.empty_like(t).pin_memory() for t in h_in]
+    h_out[2] = h_in[2]  # in place
+    out, temp = g.gbs_sort_keys_host_batch(h_in, h_out, descending=descending, return_temp=True)
+    assert g.gbs_get_status(temp) == g.GBS_OK  # synchronises the stream
+    for i, k in enumerate(keys):
+        assert out[i].data_ptr() == h_out[i].data_ptr()
+        assert np.array_equal(_u(out[i].numpy()), _u(oracle.sort_keys(k, descending=descending))), i
+        if i != 2:
+            assert np.array_equal(_u(h_in[i].numpy()), _u(k))  # inputs untouched
+
+
+@pytest.mark.parametrize("bits", [(4, 20), (8, 8), (0, 32)])
+def test_sort_keys_host_batch_bit_ranges_and_reused_work_buffer(g, bits):
+    sizes = [3 * TILE32 + 7, 40000, 10]
+    keys = [with_ties(np.uint32, n, 500 + n) for n in sizes]
+    h_in = [torch.from_numpy(k.copy()).pin_memory() for k in keys]
+    out, temp = g.gbs_sort_keys_host_batch(h_in, begin_bit=bits[0], end_bit=bits[1], return_temp=True)
+    out2 = g.gbs_sort_keys_host_batch(h_in, begin_bit=bits[0], end_bit=bits[1], temp=temp)
+    assert g.gbs_get_status(temp) == g.GBS_OK
+    for i, k in enumerate(keys):
+        want = oracle.sort_keys(k, bits[0], bits[1])
+        assert np.array_equal(out[i].numpy(), want) and np.array_equal(out2[i].numpy(), want)
+
+
+def test_sort_keys_host_batch_empty_and_ordering(g):
+    # an empty batch clears the header and enqueues nothing else
+    _, temp = g.gbs_sort_keys_host_batch([], return_temp=True)
+    assert g.gbs_get_status(temp) == g.GBS_OK
+    # the copies wait for work enqueued on the stream before the call: the input is written by a device
+    # copy just before, and the output is read right after the stream (and nothing else) is synchronised
+    n = 2 * TILE32 + 5
+    keys = wl.uniform_u32(n, 77)
+    src = _dev(keys.view(np.int32))
+    h = torch.empty(n, dtype=torch.int32).pin_memory()
+    h.copy_(src, non_blocking=True)  # device-to-host copy enqueued on the current stream
+    out = g.gbs_sort_keys_host_batch([h], key_type=g.GBS_U32)
+    torch.cuda.current_stream().synchronize()
+    assert np.array_equal(out[0].numpy().view(np.uint32), oracle.sort_keys(keys))
+
+
 def test_all_passes_trivial_and_skipped_passes(g):
     n = 3 * TILE32 + 9
     eq = wl.all_equal_u32(n, 1)
