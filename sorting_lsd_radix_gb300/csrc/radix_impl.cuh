@@ -529,7 +529,7 @@ __device__ __forceinline__ void wait_phase(uint64_t *bar, uint32_t parity, const
 }
 
 #ifndef LOOKBACK_WINDOW
-#define LOOKBACK_WINDOW 8
+#define LOOKBACK_WINDOW 6
 #endif
 
 // Status words of predecessors lb_next, lb_next - 1, ... for digit d; a
