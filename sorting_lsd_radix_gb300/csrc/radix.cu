@@ -7,15 +7,14 @@
 namespace gbs {
 
 // Keys per tile of each launch shape (the pass kernel's tuning macros).
+template <typename K, int VB> constexpr uint32_t shape_tile() {
+    return (uint32_t)PassShape<K, VB>::THREADS * PassShape<K, VB>::ITEMS;
+}
+
 uint32_t radix_tile_keys(int key_bytes, int val_bytes) {
-    if (key_bytes == 8) {
-        if (val_bytes == 8) return (uint32_t)GBS_U64_V64_THREADS * GBS_U64_V64_ITEMS;
-        return val_bytes ? (uint32_t)GBS_U64_PAIR_THREADS * GBS_U64_PAIR_ITEMS
-                         : (uint32_t)GBS_U64_THREADS * GBS_U64_ITEMS;
-    }
-    if (val_bytes == 8) return (uint32_t)GBS_U32_V64_THREADS * GBS_U32_V64_ITEMS;
-    return val_bytes ? (uint32_t)GBS_U32_PAIR_THREADS * GBS_U32_PAIR_ITEMS
-                     : (uint32_t)GBS_U32_THREADS * GBS_U32_ITEMS;
+    if (key_bytes == 8)
+        return val_bytes == 8 ? shape_tile<uint64_t, 8>() : val_bytes ? shape_tile<uint64_t, 4>() : shape_tile<uint64_t, 0>();
+    return val_bytes == 8 ? shape_tile<uint32_t, 8>() : val_bytes ? shape_tile<uint32_t, 4>() : shape_tile<uint32_t, 0>();
 }
 
 cudaError_t launch_histograms(const RadixJob &job, cudaStream_t stream, int *launches) {

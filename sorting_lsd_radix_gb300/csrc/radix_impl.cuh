@@ -751,18 +751,23 @@ __device__ __forceinline__ void pass_tile(PassSmem<K, VB, THREADS, ITEMS> &sm, c
         store_tile<false, BYTE, K, VB, THREADS>(sm.keys, sm.vals, sm.binoff, valid, kdst, vdst, prm, tid);
 }
 
-// Launch shapes of the pass kernel (threads per CTA x keys per thread).  Every
-// shape keeps PASS_THREADS_PER_SM threads resident per SM (64 registers per
-// thread); smaller CTAs give more independent tiles per SM, whose latency-bound
-// phases (tile load, look-back, scatter) then overlap other tiles' ranking.
-#ifndef GBS_PASS_THREADS_PER_SM
-#define GBS_PASS_THREADS_PER_SM 1024
-#endif
+// Launch shapes of the pass kernel: threads per CTA x keys per thread, and the
+// CTAs kept resident per SM (which sets the register budget: 65536 / (CTAs x
+// threads), in steps of 8).  Four 256-thread CTAs (64 registers) suit u32
+// keys.  Values and 64-bit keys need more registers per key: three CTAs at 80
+// registers then hold more keys per tile without spilling, which measured
+// faster than four smaller tiles with spills or two larger ones.  More,
+// smaller tiles per SM let the latency-bound phases (tile load, look-back,
+// scatter) overlap other tiles' ranking; larger tiles spend less on per-tile
+// costs.
 #ifndef GBS_U32_THREADS
 #define GBS_U32_THREADS 256
 #endif
 #ifndef GBS_U32_ITEMS
 #define GBS_U32_ITEMS 32
+#endif
+#ifndef GBS_U32_CTAS
+#define GBS_U32_CTAS 4
 #endif
 #ifndef GBS_U32_PAIR_THREADS
 #define GBS_U32_PAIR_THREADS 256
@@ -770,33 +775,69 @@ __device__ __forceinline__ void pass_tile(PassSmem<K, VB, THREADS, ITEMS> &sm, c
 #ifndef GBS_U32_PAIR_ITEMS
 #define GBS_U32_PAIR_ITEMS 32
 #endif
+#ifndef GBS_U32_PAIR_CTAS
+#define GBS_U32_PAIR_CTAS 3
+#endif
 #ifndef GBS_U64_THREADS
 #define GBS_U64_THREADS 256
 #endif
 #ifndef GBS_U64_ITEMS
-#define GBS_U64_ITEMS 20
+#define GBS_U64_ITEMS 24
+#endif
+#ifndef GBS_U64_CTAS
+#define GBS_U64_CTAS 3
 #endif
 #ifndef GBS_U64_PAIR_THREADS
 #define GBS_U64_PAIR_THREADS 256
 #endif
 #ifndef GBS_U64_PAIR_ITEMS
-#define GBS_U64_PAIR_ITEMS 14
+#define GBS_U64_PAIR_ITEMS 20
+#endif
+#ifndef GBS_U64_PAIR_CTAS
+#define GBS_U64_PAIR_CTAS 3
 #endif
 // 64-bit values
 #ifndef GBS_U32_V64_THREADS
 #define GBS_U32_V64_THREADS 256
 #endif
 #ifndef GBS_U32_V64_ITEMS
-#define GBS_U32_V64_ITEMS 16
+#define GBS_U32_V64_ITEMS 20
+#endif
+#ifndef GBS_U32_V64_CTAS
+#define GBS_U32_V64_CTAS 3
 #endif
 #ifndef GBS_U64_V64_THREADS
 #define GBS_U64_V64_THREADS 256
 #endif
 #ifndef GBS_U64_V64_ITEMS
-#define GBS_U64_V64_ITEMS 12
+#define GBS_U64_V64_ITEMS 16
 #endif
+#ifndef GBS_U64_V64_CTAS
+#define GBS_U64_V64_CTAS 3
+#endif
+
+template <typename K, int VB> struct PassShape;
+template <> struct PassShape<uint32_t, 0> {
+    static constexpr int THREADS = GBS_U32_THREADS, ITEMS = GBS_U32_ITEMS, CTAS = GBS_U32_CTAS;
+};
+template <> struct PassShape<uint32_t, 4> {
+    static constexpr int THREADS = GBS_U32_PAIR_THREADS, ITEMS = GBS_U32_PAIR_ITEMS, CTAS = GBS_U32_PAIR_CTAS;
+};
+template <> struct PassShape<uint32_t, 8> {
+    static constexpr int THREADS = GBS_U32_V64_THREADS, ITEMS = GBS_U32_V64_ITEMS, CTAS = GBS_U32_V64_CTAS;
+};
+template <> struct PassShape<uint64_t, 0> {
+    static constexpr int THREADS = GBS_U64_THREADS, ITEMS = GBS_U64_ITEMS, CTAS = GBS_U64_CTAS;
+};
+template <> struct PassShape<uint64_t, 4> {
+    static constexpr int THREADS = GBS_U64_PAIR_THREADS, ITEMS = GBS_U64_PAIR_ITEMS, CTAS = GBS_U64_PAIR_CTAS;
+};
+template <> struct PassShape<uint64_t, 8> {
+    static constexpr int THREADS = GBS_U64_V64_THREADS, ITEMS = GBS_U64_V64_ITEMS, CTAS = GBS_U64_V64_CTAS;
+};
+
 template <typename K, int VB, int THREADS, int ITEMS, bool BYTE, typename SW>
-__global__ void __launch_bounds__(THREADS, GBS_PASS_THREADS_PER_SM / THREADS)
+__global__ void __launch_bounds__(THREADS, PassShape<K, VB>::CTAS)
     onesweep_pass_kernel(const PassParams prm) {
     constexpr bool PAIRS = VB != 0;
     using V = ValueT<VB>;
@@ -1043,7 +1084,7 @@ cudaError_t launch_passes(const RadixJob &job, cudaStream_t stream, int *launche
     prm.fault_pass = job.fault_pass;
     prm.fault_tile = job.fault_tile;
     prm.digit_base = job.digit_base;
-    prm.prefetch_ahead = (uint32_t)(device_sms() * (GBS_PASS_THREADS_PER_SM / THREADS) / 2);
+    prm.prefetch_ahead = (uint32_t)(device_sms() * PassShape<K, VB>::CTAS / 2);
     for (int p = 0; p < job.num_passes; ++p) {
         prm.pass = p;
         prm.shift = job.begin_bit + 8 * p;
@@ -1061,14 +1102,19 @@ cudaError_t launch_passes(const RadixJob &job, cudaStream_t stream, int *launche
 }
 
 // Every digit pass of a radix job, with status words of type SW.
+template <typename K, int VB, typename SW>
+cudaError_t launch_shape(const RadixJob &job, cudaStream_t stream, int *launches) {
+    return launch_passes<K, VB, PassShape<K, VB>::THREADS, PassShape<K, VB>::ITEMS, SW>(job, stream, launches);
+}
+
 template <typename SW> cudaError_t launch_all_passes(const RadixJob &job, cudaStream_t stream, int *launches) {
     if (job.key_bytes == 8)
-        return job.val_bytes == 8 ? launch_passes<uint64_t, 8, GBS_U64_V64_THREADS, GBS_U64_V64_ITEMS, SW>(job, stream, launches)
-               : job.val_bytes    ? launch_passes<uint64_t, 4, GBS_U64_PAIR_THREADS, GBS_U64_PAIR_ITEMS, SW>(job, stream, launches)
-                                  : launch_passes<uint64_t, 0, GBS_U64_THREADS, GBS_U64_ITEMS, SW>(job, stream, launches);
-    return job.val_bytes == 8 ? launch_passes<uint32_t, 8, GBS_U32_V64_THREADS, GBS_U32_V64_ITEMS, SW>(job, stream, launches)
-           : job.val_bytes    ? launch_passes<uint32_t, 4, GBS_U32_PAIR_THREADS, GBS_U32_PAIR_ITEMS, SW>(job, stream, launches)
-                              : launch_passes<uint32_t, 0, GBS_U32_THREADS, GBS_U32_ITEMS, SW>(job, stream, launches);
+        return job.val_bytes == 8 ? launch_shape<uint64_t, 8, SW>(job, stream, launches)
+               : job.val_bytes    ? launch_shape<uint64_t, 4, SW>(job, stream, launches)
+                                  : launch_shape<uint64_t, 0, SW>(job, stream, launches);
+    return job.val_bytes == 8 ? launch_shape<uint32_t, 8, SW>(job, stream, launches)
+           : job.val_bytes    ? launch_shape<uint32_t, 4, SW>(job, stream, launches)
+                              : launch_shape<uint32_t, 0, SW>(job, stream, launches);
 }
 
 }  // namespace

@@ -49,6 +49,18 @@ def _query(lib, fn, *args):
     return st, need.value
 
 
+def test_parity_sizes_straddle_the_launch_shapes_tiles(lib):
+    from tests import test_gpu_parity as tp
+    assert gbsort.gbs_debug_radix_tile_keys(4) == tp.TILE32
+    assert gbsort.gbs_debug_radix_tile_keys(4, value_bytes=4) == tp.TILE32
+    assert gbsort.gbs_debug_radix_tile_keys(8) == tp.TILE64
+    assert gbsort.gbs_debug_radix_tile_keys(8, value_bytes=4) == tp.TILE64P
+    assert gbsort.gbs_debug_radix_tile_keys(4, value_bytes=8) == tp.TILE64P
+    assert gbsort.gbs_debug_radix_tile_keys(8, value_bytes=8) == tp.TILE64V64
+    for t in (tp.TILE32, tp.TILE64, tp.TILE64P, tp.TILE64V64):
+        assert {t - 1, t, t + 1} <= set(tp.SIZES)
+
+
 def test_temp_query_sizes(lib):
     n = 10**6
     st, need = _query(lib, "gbs_sort_keys", gbsort.GBS_U32, None, None, n, 0, 32, 0, None)

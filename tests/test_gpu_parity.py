@@ -56,12 +56,14 @@ def with_ties(dtype, n, seed, k=37):
 
 
 # Radix tile sizes of the launch shapes: 8192 keys (u32 keys and u32 pairs),
-# 5120 (u64 keys), 3584 (u64 keys with u32 values).  The sizes straddle each
-# boundary, span several tiles with a ragged tail, and cross the bitonic/radix
-# switch at 16384 keys.
+# 6144 (u64 keys), 5120 (u64 keys with u32 values, u32 keys with u64 values),
+# 4096 (u64 keys with u64 values).  The sizes straddle each boundary, span
+# several tiles with a ragged tail, and cross the bitonic/radix switch at 16384
+# keys.
 TILE32 = 8192
-TILE64 = 5120
-TILE64P = 3584
+TILE64 = 6144
+TILE64P = 5120
+TILE64V64 = 4096
 SIZES = [0, 1, 2, 31, 32, 33, 1023, TILE64P - 1, TILE64P, TILE64P + 1, 4095, 4096, 4097, TILE64 - 1, TILE64,
          TILE64 + 1, TILE32 - 1, TILE32, TILE32 + 1, 16383, 16384, 16385, 3 * TILE32 + 5, 5 * TILE64 + 3,
          7 * TILE64P + 9, (1 << 16) + 7, (1 << 20) + 3]
