@@ -579,6 +579,8 @@ SECONDARY = {
     "f64_2p27_radix11": ("sort_keys f64 n=2^27 N(0,1000) with signed zeros and infinities, 11-bit-digit prototype",
                          _sec_radix_keys(lambda n: wl.normal_mix_f64(n, wl.seed_for(6, 0)), 1 << 27, "f64",
                                          radix_bits=11)),
+    "u32_2p30": ("sort_keys u32 n=2^30 uniform (4 GiB; from 2^29 keys on the look-back status words are 64-bit)",
+                 _sec_radix_keys(lambda n: wl.uniform_u32(n, wl.seed_for(3, 2)), 1 << 30, "u32")),
     "u32_1e8_bits0_16": ("sort_keys u32 n=1e8 uniform, bits [0,16)",
                          _sec_radix_keys(lambda n: wl.uniform_u32(n, SEED), N_KEYS, "u32", 0, 16)),
     "f32_2p28": ("sort_keys f32 n=2^28, N(0,1000) with signed zeros and infinities",
