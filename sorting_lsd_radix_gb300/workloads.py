@@ -176,6 +176,37 @@ def _normal_mix(n: int, seed: int, sigma: float, dtype) -> np.ndarray:
     return out
 
 
+def _to_signed64(x: int) -> int:
+    x &= 0xFFFFFFFFFFFFFFFF
+    return x - (1 << 64) if x >> 63 else x
+
+
+def uniform_u32_torch(n: int, seed: int, device, chunk: int = 1 << 26):
+    """uniform_u32(n, seed) drawn with torch on `device` (the same SplitMix64 stream, bit for bit),
+    returned as an int32 tensor holding the uint32 bit patterns.  For arrays too large to draw on
+    the host in reasonable time; int64 arithmetic wraps modulo 2^64, and right shifts are made
+    logical by masking."""
+    import torch
+    out = torch.empty(n, dtype=torch.int32, device=device)
+    gamma, m1, m2 = (_to_signed64(int(v)) for v in (GAMMA, _M1, _M2))
+    s64 = _to_signed64(seed)
+
+    def lsr(z, k):
+        return (z >> k) & ((1 << (64 - k)) - 1)
+
+    for start in range(0, n, chunk):
+        c = min(chunk, n - start)
+        z = torch.arange(start + 1, start + c + 1, dtype=torch.int64, device=device) * gamma + s64
+        z ^= lsr(z, 30)
+        z *= m1
+        z ^= lsr(z, 27)
+        z *= m2
+        z ^= lsr(z, 31)
+        hi = lsr(z, 32)  # in [0, 2^32)
+        out[start:start + c] = torch.where(hi >= (1 << 31), hi - (1 << 32), hi).to(torch.int32)
+    return out
+
+
 def zero_one_patterns(bits: int) -> np.ndarray:
     """Every 0-1 vector of length ``bits`` (2^bits rows, one per pattern), as uint32."""
     codes = np.arange(1 << bits, dtype=np.uint32)

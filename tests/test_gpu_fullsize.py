@@ -142,3 +142,46 @@ def test_wide_status_2p30_plus_7_u32(g, dist):
     if dist == "and4":
         assert ((want & np.uint32(0xFF)) == 0).sum() > (1 << 29)  # digit 0 of pass 0 passes 2^29 keys
     assert np.array_equal(got, want)
+
+
+def _as_signed_order(x):
+    """int32 tensor of uint32 bit patterns -> int32 values in the same order as the unsigned keys."""
+    return x ^ torch.tensor(-(1 << 31), dtype=torch.int32, device=x.device)
+
+
+def test_largest_radix_size_u32(g):
+    """The largest radix sort the library accepts: 2^32 - 1 u32 keys (16 GiB, 524,288 tiles,
+    64-bit status words), drawn on the device (the same SplitMix64 stream as the host generator).
+    The oracle cannot sort 2^32 keys in test time, so the result is checked by properties that hold
+    at any size, with torch operations only: the output is non-decreasing; each of its four byte
+    positions has the input's value counts; and at sampled positions i the output value v satisfies
+    #(keys < v) <= i < #(keys <= v), which makes v the i-th smallest key."""
+    n = g.GBS_MAX_RADIX_KEYS
+    keys = wl.uniform_u32_torch(n, wl.seed_for(3, 13), "cuda")
+    # the device draws are the host stream's (checked on a slice)
+    assert np.array_equal(keys[:4096].cpu().numpy().view(np.uint32), wl.uniform_u32(4096, wl.seed_for(3, 13)))
+    out, temp = g.gbs_sort_keys(keys, return_temp=True, key_type=g.GBS_U32)
+    assert g.gbs_get_status(temp) == g.GBS_OK
+    del temp
+    torch.cuda.empty_cache()
+    chunk = 1 << 28
+    for start in range(0, n - 1, chunk):
+        a = _as_signed_order(out[start:min(n, start + chunk + 1)])
+        assert bool((a[1:] >= a[:-1]).all()), start
+    for p in range(4):
+        hi, ho = torch.zeros(256, dtype=torch.int64, device="cuda"), torch.zeros(256, dtype=torch.int64, device="cuda")
+        for start in range(0, n, chunk):
+            stop = min(n, start + chunk)
+            hi += torch.bincount(((keys[start:stop] >> (8 * p)) & 0xFF).to(torch.int64), minlength=256)
+            ho += torch.bincount(((out[start:stop] >> (8 * p)) & 0xFF).to(torch.int64), minlength=256)
+        assert torch.equal(hi, ho), p
+    rng = np.random.default_rng(wl.seed_for(3, 14))
+    for i in [0, n - 1] + [int(x) for x in rng.integers(0, n, 6)]:
+        v = _as_signed_order(out[i:i + 1])
+        below = at_most = 0
+        for start in range(0, n, chunk):
+            k = _as_signed_order(keys[start:min(n, start + chunk)])
+            below += int((k < v).sum())
+            at_most += int((k <= v).sum())
+        assert below <= i < at_most, i
+

@@ -410,3 +410,13 @@ def test_splitmix64_published_outputs():
     # first three outputs of SplitMix64 from state 0 (Vigna's reference splitmix64.c)
     assert [int(x) for x in wl.splitmix64(0, 3)] == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4,
                                                       0x06C45D188009454F]
+
+
+def test_torch_generator_draws_the_host_stream():
+    torch = pytest.importorskip("torch")
+    # the published first output of state 0, through the torch form (high 32 bits)
+    assert int(wl.uniform_u32_torch(1, 0, "cpu").numpy().view(np.uint32)[0]) == 0xE220A839
+    for n, chunk in ((1, 1 << 20), (100003, 4096), (1 << 20, 1 << 18)):
+        seed = wl.seed_for(3, 20)
+        got = wl.uniform_u32_torch(n, seed, "cpu", chunk=chunk).numpy().view(np.uint32)
+        assert np.array_equal(got, wl.uniform_u32(n, seed))
