@@ -556,13 +556,16 @@ __device__ __forceinline__ void add_window(const SW (&sw)[W], uint32_t st_agg, u
 #pragma unroll
     for (int w = 0; w < W; ++w) {
         const uint32_t rel = (uint32_t)(sw[w] >> CB) - st_agg;  // 0: aggregate, 1: inclusive prefix
-        if (rel > 1u) break;
-        excl += (uint32_t)(sw[w] & CM);
-        used = w + 1;
-        if (rel == 1u) {
-            done = true;
+        if (rel != 0u) {  // one test on the common path, an aggregate
+            if (rel == 1u) {
+                excl += (uint32_t)(sw[w] & CM);
+                used = w + 1;
+                done = true;
+            }
             break;
         }
+        excl += (uint32_t)(sw[w] & CM);
+        used = w + 1;
     }
 }
 
