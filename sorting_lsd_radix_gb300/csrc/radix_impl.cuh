@@ -550,21 +550,26 @@ __device__ __forceinline__ void add_window(const SW (&sw)[W], uint32_t st_agg, u
                                            bool &done) {
     constexpr int CB = StatusWord<SW>::COUNT_BITS;
     constexpr SW CM = StatusWord<SW>::COUNT_MASK;
-    // this pass's states are st_agg (aggregate) and st_agg + 1 (inclusive prefix)
+    // this pass's states are st_agg (aggregate) and st_agg + 1 (inclusive
+    // prefix).  Subtracting the aggregate state's bits leaves the count of an
+    // aggregate and a value above COUNT_MASK for any other word (unsigned
+    // wrap-around included), so one subtraction both tests and extracts.
+    const SW agg = (SW)st_agg << CB;
     used = 0;
     done = false;
 #pragma unroll
     for (int w = 0; w < W; ++w) {
-        const uint32_t rel = (uint32_t)(sw[w] >> CB) - st_agg;  // 0: aggregate, 1: inclusive prefix
-        if (rel != 0u) {  // one test on the common path, an aggregate
-            if (rel == 1u) {
-                excl += (uint32_t)(sw[w] & CM);
+        const SW c = sw[w] - agg;
+        if (c > CM) {  // not an aggregate of this pass: an inclusive prefix ends the walk
+            const SW ci = c - ((SW)1 << CB);
+            if (ci <= CM) {
+                excl += (uint32_t)ci;
                 used = w + 1;
                 done = true;
             }
             break;
         }
-        excl += (uint32_t)(sw[w] & CM);
+        excl += (uint32_t)c;
         used = w + 1;
     }
 }
