@@ -603,17 +603,34 @@ __device__ __forceinline__ uint32_t lookback_excl(const PassParams &prm, Header 
     return excl;
 }
 
-// The tile's count of digit d (thread d < 256) from the warps' counters, which
-// become each warp's exclusive offset within the digit's keys.
-template <int WARPS> __device__ __forceinline__ uint32_t tile_digit_count(uint32_t (*whist)[256], int d) {
+// The tile's count of digit d (thread d < 256), the sum of the warps'
+// counters.  WRITE_RUN: the counters also become each warp's exclusive offset
+// within the digit's keys (else warp_offsets does that after the tile scan,
+// with one store per counter instead of two).
+template <int WARPS, bool WRITE_RUN>
+__device__ __forceinline__ uint32_t tile_digit_count(uint32_t (*whist)[256], int d) {
     uint32_t run = 0;
 #pragma unroll 4
     for (int w = 0; w < WARPS; ++w) {
         const uint32_t c = whist[w][d];
-        whist[w][d] = run;
+        if (WRITE_RUN) whist[w][d] = run;
         run += c;
     }
     return run;
+}
+
+// Sorted-tile slot of each warp's first key of digit d, from the digit's
+// offset in the tile (local).  RUN_WRITTEN: the counters already hold the
+// warps' exclusive offsets within the digit.
+template <int WARPS, bool RUN_WRITTEN>
+__device__ __forceinline__ void warp_offsets(uint32_t (*whist)[256], int d, uint32_t local) {
+    uint32_t run = local;
+#pragma unroll 4
+    for (int w = 0; w < WARPS; ++w) {
+        const uint32_t c = whist[w][d];
+        whist[w][d] = RUN_WRITTEN ? c + local : run;
+        run += c;
+    }
 }
 
 // Source and destination buffers of active pass number k of A.  The last
@@ -677,18 +694,22 @@ __device__ __forceinline__ void pass_tile(PassSmem<K, VB, THREADS, ITEMS> &sm, c
     // ---- tile digit counts, warp offsets, publish the aggregate ------------
     uint32_t cnt = 0;
     constexpr int CB = StatusWord<SW>::COUNT_BITS;
+    // 32-bit keys write the warps' offsets once, after the tile scan; for
+    // 64-bit keys that form measured slower (its register allocation spills
+    // more), so they write the offsets within the digit first and add the
+    // tile offset after the scan
+    constexpr bool RUN_FIRST = sizeof(K) == 8;
     const bool faulty = (prm.fault_pass == prm.pass) && (prm.fault_tile == tile);
     SW *my_status = reinterpret_cast<SW *>(prm.status) + (size_t)tile * 256;
     if (tid < 256) {
-        cnt = tile_digit_count<WARPS>(sm.whist, tid);
+        cnt = tile_digit_count<WARPS, RUN_FIRST>(sm.whist, tid);
         if (!faulty) st_relaxed_gpu(my_status + tid, ((SW)(tile == 0 ? st_inc : st_agg) << CB) | cnt);
     }
     // (wsum is not written again before the barrier after the offsets)
     const uint32_t local = excl_scan_256<false>(cnt, sm.wsum);
     if (tid < 256) {
         // sorted-tile slot of each warp's first key of digit tid
-#pragma unroll 4
-        for (int w = 0; w < WARPS; ++w) sm.whist[w][tid] += local;
+        warp_offsets<WARPS, RUN_FIRST>(sm.whist, tid, local);
     }
     __syncthreads();
 
