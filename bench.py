@@ -367,7 +367,7 @@ def run_gbsort(args):
         # the one-at-a-time figure above is kept beside it.
         outs = [h_out, torch.empty_like(h_in).pin_memory()]
         _, btemp = gbsort.gbs_sort_keys_host_batch([h_in, h_in], outs, return_temp=True)
-        kb = 2 * max(2, min(args.steps, 12) // 2)
+        kb = 32  # arrays per call: the pipeline's fill and drain (about one step) are spread over 32
         ins_b, outs_b = [h_in] * kb, [outs[i % 2] for i in range(kb)]
         gbsort.gbs_sort_keys_host_batch(ins_b, outs_b, temp=btemp)  # warm-up
         barrier()
