@@ -165,6 +165,19 @@ def test_host_batch_rejects_bad_arguments(lib):
                                         None) == gbsort.GBS_ERR_INVALID_ARG
 
 
+def test_host_batch_binding_checks_its_arguments(lib):
+    torch = pytest.importorskip("torch")
+    a32, b32 = torch.zeros(3, dtype=torch.int32), torch.zeros(5, dtype=torch.int32)
+    with pytest.raises(ValueError):  # one dtype for the whole batch
+        gbsort.gbs_sort_keys_host_batch([a32, torch.zeros(3, dtype=torch.int64)])
+    with pytest.raises(ValueError):  # one output per input
+        gbsort.gbs_sort_keys_host_batch([a32, b32], [torch.zeros(3, dtype=torch.int32)])
+    with pytest.raises(ValueError):  # outputs shaped like their inputs
+        gbsort.gbs_sort_keys_host_batch([a32, b32], [torch.zeros(3, dtype=torch.int32), torch.zeros(4, dtype=torch.int32)])
+    with pytest.raises(ValueError):  # contiguous host tensors only
+        gbsort.gbs_sort_keys_host_batch([a32[::2]])
+
+
 def _offsets(values):
     a = (ctypes.c_uint64 * len(values))(*values)
     return a
